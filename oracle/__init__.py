@@ -1,0 +1,142 @@
+"""Test infrastructure: ctypes wrapper around the float64 CPU oracle (oracle.c).
+
+Only tests/, ``__graft_entry__.smoke()`` and bench.py's CPU-baseline leg may
+import this package.  The product path (``group_affine_bit_gb300`` and
+``libaffqmm``) never does; it fails loudly when its own CUDA library is
+missing instead of falling back to anything here.
+
+All arrays are numpy: codes uint8 [N,K]; scales, biases uint16 (bf16 bit
+patterns) [N,K/g]; x uint16 [M,K].  See oracle.h for the arithmetic.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "oracle.c")
+LIB = os.path.join(HERE, "liboracle.so")
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def compile_oracle(src: str = SRC, out: str = LIB) -> str:
+    """Compile oracle.c (or a copy of it) into a shared library with gcc."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", "-I", HERE, src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _ptr(a: np.ndarray, t):
+    return a.ctypes.data_as(t)
+
+
+class Oracle:
+    """Typed calls into one compiled oracle library."""
+
+    def __init__(self, path: str = LIB):
+        if path == LIB and (not os.path.exists(LIB) or
+                            os.path.getmtime(LIB) < os.path.getmtime(SRC)):
+            compile_oracle()
+        self.path = path
+        lib = ctypes.CDLL(path)
+        lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+        lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_from_f32_bits.restype = None
+        lib.oracle_bf16_from_f32_bits.argtypes = [_u32p, _u16p, ctypes.c_size_t]
+        lib.oracle_dequant_one.restype = ctypes.c_uint16
+        lib.oracle_dequant_one.argtypes = [ctypes.c_uint32, ctypes.c_uint16, ctypes.c_uint16]
+        lib.oracle_dequant.restype = ctypes.c_int
+        lib.oracle_dequant.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64,
+                                       _u8p, _u16p, _u16p, _u16p]
+        lib.oracle_qmm.restype = ctypes.c_int
+        lib.oracle_qmm.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64,
+                                   _u16p, _u8p, _u16p, _u16p, _f64p, ctypes.c_int]
+        lib.oracle_qmm_groupsum.restype = ctypes.c_int
+        lib.oracle_qmm_groupsum.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64,
+                                            _u16p, _u8p, _u16p, _u16p, _f64p, _f64p]
+        self.lib = lib
+
+    # -- bf16 -----------------------------------------------------------
+    def bf16_from_double(self, v: float) -> int:
+        return int(self.lib.oracle_bf16_from_double(float(v)))
+
+    def bf16_to_double(self, h: int) -> float:
+        return float(self.lib.oracle_bf16_to_double(int(h) & 0xFFFF))
+
+    def bf16_from_f32_bits(self, bits: np.ndarray) -> np.ndarray:
+        bits = np.ascontiguousarray(bits, dtype=np.uint32)
+        out = np.empty(bits.shape, dtype=np.uint16)
+        self.lib.oracle_bf16_from_f32_bits(_ptr(bits, _u32p), _ptr(out, _u16p), bits.size)
+        return out
+
+    # -- dequant ----------------------------------------------------------
+    def dequant_one(self, q: int, s: int, b: int) -> int:
+        return int(self.lib.oracle_dequant_one(int(q), int(s) & 0xFFFF, int(b) & 0xFFFF))
+
+    def dequant(self, bits, group, codes, scales, biases) -> np.ndarray:
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        biases = np.ascontiguousarray(biases, dtype=np.uint16)
+        N, K = codes.shape
+        out = np.empty((N, K), dtype=np.uint16)
+        rc = self.lib.oracle_dequant(bits, group, N, K, _ptr(codes, _u8p),
+                                     _ptr(scales, _u16p), _ptr(biases, _u16p), _ptr(out, _u16p))
+        if rc:
+            raise ValueError(f"oracle_dequant rejected its arguments (rc={rc})")
+        return out
+
+    # -- projection ---------------------------------------------------------
+    def qmm(self, bits, group, x, codes, scales, biases, nthreads: int = 1) -> np.ndarray:
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        biases = np.ascontiguousarray(biases, dtype=np.uint16)
+        M, K = x.shape
+        N, K2 = codes.shape
+        if K != K2:
+            raise ValueError("x and codes disagree on K")
+        y = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.oracle_qmm(bits, group, M, N, K, _ptr(x, _u16p), _ptr(codes, _u8p),
+                                 _ptr(scales, _u16p), _ptr(biases, _u16p), _ptr(y, _f64p),
+                                 int(nthreads))
+        if rc:
+            raise ValueError(f"oracle_qmm rejected its arguments (rc={rc})")
+        return y
+
+    def qmm_groupsum(self, bits, group, x, codes, scales, biases):
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        biases = np.ascontiguousarray(biases, dtype=np.uint16)
+        M, K = x.shape
+        N = codes.shape[0]
+        y = np.empty((M, N), dtype=np.float64)
+        mag = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.oracle_qmm_groupsum(bits, group, M, N, K, _ptr(x, _u16p), _ptr(codes, _u8p),
+                                          _ptr(scales, _u16p), _ptr(biases, _u16p),
+                                          _ptr(y, _f64p), _ptr(mag, _f64p))
+        if rc:
+            raise ValueError(f"oracle_qmm_groupsum rejected its arguments (rc={rc})")
+        return y, mag
+
+
+_DEFAULT = None
+
+
+def load() -> Oracle:
+    """The oracle built from oracle.c in this directory (compiled on first use)."""
+    global _DEFAULT
+    if _DEFAULT is None:
+        _DEFAULT = Oracle()
+    return _DEFAULT

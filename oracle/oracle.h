@@ -1,0 +1,77 @@
+/*
+ * oracle.h -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, float64 CPU oracle for the MLX-style group-affine quantized
+ * linear projection.  It exists so that tests/ and the bench's CPU baseline
+ * can check the CUDA library against an independent implementation.  Nothing
+ * in the product path (the libaffqmm library and its Python binding) may
+ * include, link or call this code, and this code includes nothing of theirs.
+ *
+ * Inputs are the canonical, unpacked form of an affine table:
+ *   codes  q[N,K]   one code per byte, 0 <= q < 2^bits
+ *   scales s[N,K/g] bf16 bit patterns (uint16), row-major
+ *   biases b[N,K/g] bf16 bit patterns (uint16), row-major
+ *   x[M,K]          bf16 bit patterns, row-major
+ * Group j of row n covers k in [j*g, (j+1)*g).
+ *
+ * Sources (web pages on the TensorFold project):
+ *  - "Gemma 4 12B on the native Metal engine" (PR #975), the commit that makes
+ *    the prompt GEMM dequantize each weight as bf16(fma(scale, code, bias)) with
+ *    one rounding, as mlx-lm's quantized matmul does, and accumulate over the
+ *    whole depth; the same page's lane kernels that keep codes exact and use
+ *    precomputed group sums (the "reg variant" commit).
+ *  - "cuda gemma4: images on the 12B ..." (PR #1183), the embed_rows commit
+ *    (MLX affine tables at 2/3/4/5/6/8 bits, groups of 32/64/128) and the
+ *    bf16 rounding commit (signed zero from underflow, subnormal ties, the
+ *    normal boundary, overflow to both infinities).
+ *
+ * Every function returns 0 on success and a negative value on a bad argument.
+ */
+#ifndef GAB_ORACLE_H
+#define GAB_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* bf16 round-to-nearest-even of a double: NaN stays NaN (0x7FC0, sign kept),
+ * overflow gives +-inf, underflow keeps the sign (-2^-135 -> 0x8000). */
+uint16_t oracle_bf16_from_double(double v);
+/* The exact value of a bf16 bit pattern. */
+double oracle_bf16_to_double(uint16_t h);
+/* Encode n fp32 bit patterns (as uint32) to bf16 through the double path. */
+void oracle_bf16_from_f32_bits(const uint32_t* in, uint16_t* out, size_t n);
+
+/* One weight: bf16(s*q + b) with a single rounding of the exact value. */
+uint16_t oracle_dequant_one(uint32_t q, uint16_t s, uint16_t b);
+
+/* W[n,k] = bf16(s[n,k/g]*q[n,k] + b[n,k/g]), all N*K weights. */
+int oracle_dequant(int bits, int group, int64_t N, int64_t K,
+                   const uint8_t* codes, const uint16_t* scales,
+                   const uint16_t* biases, uint16_t* w_out);
+
+/* y[m,n] = sum over k ascending of W[n,k]*x[m,k], in double.
+ * y_out is [M,N] row-major.  nthreads <= 1 runs on the calling thread;
+ * otherwise output rows n are split into nthreads contiguous ranges. */
+int oracle_qmm(int bits, int group, int64_t M, int64_t N, int64_t K,
+               const uint16_t* x, const uint8_t* codes,
+               const uint16_t* scales, const uint16_t* biases,
+               double* y_out, int nthreads);
+
+/* The exact-codes form used by the pages' lane kernels:
+ * y_gs[m,n] = sum_j ( s_j * sum_{k in j} q[n,k]*x[m,k] + b_j * sum_{k in j} x[m,k] ),
+ * in double, with no bf16 rounding of the weights.  Also writes
+ * mag[m,n] = sum_k |s*q + b| * |x[m,k]| (exact weights, double), the scale the
+ * group-sum invariant is stated against.  Either output pointer may be NULL. */
+int oracle_qmm_groupsum(int bits, int group, int64_t M, int64_t N, int64_t K,
+                        const uint16_t* x, const uint8_t* codes,
+                        const uint16_t* scales, const uint16_t* biases,
+                        double* y_gs, double* mag);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
