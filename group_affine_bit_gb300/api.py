@@ -1,0 +1,218 @@
+"""Python binding of libaffqmm (include/affqmm.h): argument marshalling only.
+
+Every step of the projection runs in the library's CUDA kernels; this module
+turns torch tensors into pointers, sizes and the current CUDA stream, and
+turns status codes into exceptions.  PyTorch supplies device memory and
+streams.  There is no fallback: if libaffqmm.so is missing or cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libaffqmm.so")
+
+MAX_STACK = 8
+MAX_M = 1 << 20
+
+STATUS_NAMES = {
+    0: "AFFQMM_OK", 1: "AFFQMM_E_NULL", 2: "AFFQMM_E_BITS", 3: "AFFQMM_E_GROUP",
+    4: "AFFQMM_E_SHAPE", 5: "AFFQMM_E_ALIGN", 6: "AFFQMM_E_M", 7: "AFFQMM_E_WORKSPACE",
+    8: "AFFQMM_E_TIMEOUT", 9: "AFFQMM_E_CUDA", 10: "AFFQMM_E_ARG", 11: "AFFQMM_E_DEVICE",
+}
+
+
+class AffqmmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{what}: {self.name} ({strerror(status)})")
+
+
+class CWeight(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("packed", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libaffqmm.so (raises if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libaffqmm.so is not built ({LIB_PATH}); run group_affine_bit_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, szp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)
+        wp = ctypes.POINTER(CWeight)
+        sig = {
+            "affqmm_strerror": (ctypes.c_char_p, [i32]),
+            "affqmm_version": (i32, []),
+            "affqmm_packed_bytes": (i32, [i32, i32, i64, i64, szp]),
+            "affqmm_pack": (i32, [i32, i32, i64, i64, vp, vp, vp, vp, vp]),
+            "affqmm_workspace_bytes": (i32, [wp, i64, szp]),
+            "affqmm_workspace_bytes_stacked": (i32, [i32, wp, i64, szp]),
+            "affqmm_run": (i32, [wp, vp, i64, vp, vp, ctypes.c_size_t, vp]),
+            "affqmm_run_stacked": (i32, [i32, wp, vp, i64, ctypes.POINTER(vp), vp, ctypes.c_size_t, vp]),
+            "affqmm_dequant": (i32, [wp, vp, vp]),
+            "affqmm_workspace_status": (i32, [vp, vp]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().affqmm_strerror(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise AffqmmError(rc, what)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+@dataclass
+class PackedWeight:
+    """A packed affine table (device memory owned by the torch tensor `packed`)."""
+    bits: int
+    group: int
+    N: int
+    K: int
+    packed: torch.Tensor
+
+    def cstruct(self) -> CWeight:
+        return CWeight(self.bits, self.group, self.N, self.K, self.packed.data_ptr() if self.packed.numel() else None)
+
+
+def packed_bytes(bits: int, group: int, N: int, K: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().affqmm_packed_bytes(bits, group, N, K, ctypes.byref(out)), "affqmm_packed_bytes")
+    return out.value
+
+
+def pack(codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, bits: int, group: int,
+         stream=None) -> PackedWeight:
+    """codes uint8 [N,K]; scales, biases bf16 [N,K/group]; all on one CUDA device."""
+    N, K = codes.shape
+    for t in (codes, scales, biases):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("pack wants contiguous CUDA tensors")
+    if codes.dtype != torch.uint8 or scales.dtype != torch.bfloat16 or biases.dtype != torch.bfloat16:
+        raise ValueError("pack wants uint8 codes and bf16 scales and biases")
+    nbytes = packed_bytes(bits, group, N, K)
+    packed = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=codes.device)
+    _check(lib().affqmm_pack(bits, group, N, K, codes.data_ptr(), scales.data_ptr(), biases.data_ptr(),
+                             packed.data_ptr(), _stream_ptr(stream)), "affqmm_pack")
+    return PackedWeight(bits, group, N, K, packed)
+
+
+def workspace_bytes(w: PackedWeight, M: int) -> int:
+    out = ctypes.c_size_t(0)
+    cw = w.cstruct()
+    _check(lib().affqmm_workspace_bytes(ctypes.byref(cw), M, ctypes.byref(out)), "affqmm_workspace_bytes")
+    return out.value
+
+
+def _warray(ws):
+    arr = (CWeight * len(ws))()
+    for i, w in enumerate(ws):
+        arr[i] = w.cstruct()
+    return arr
+
+
+def workspace_bytes_stacked(ws, M: int) -> int:
+    out = ctypes.c_size_t(0)
+    arr = _warray(ws)
+    _check(lib().affqmm_workspace_bytes_stacked(len(ws), arr, M, ctypes.byref(out)),
+           "affqmm_workspace_bytes_stacked")
+    return out.value
+
+
+class Workspace:
+    """A zero-filled device buffer that grows on demand.  The library leaves it
+    zeroed after every call; calls sharing one must be stream-ordered."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.buf = torch.zeros(0, dtype=torch.uint8, device=self.device)
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_workspaces: dict = {}
+
+
+def default_workspace(device) -> Workspace:
+    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
+    if key not in _workspaces:
+        _workspaces[key] = Workspace(device)
+    return _workspaces[key]
+
+
+def _check_x(x: torch.Tensor, K: int):
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != K or not x.is_contiguous():
+        raise ValueError(f"x must be a contiguous CUDA bf16 [M, {K}] tensor")
+
+
+def run(w: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, workspace: Workspace | None = None,
+        stream=None) -> torch.Tensor:
+    """y[M, N] = bf16(x @ dequant(W)^T) with fp32 accumulation."""
+    _check_x(x, w.K)
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty(M, w.N, dtype=torch.bfloat16, device=x.device)
+    ws = workspace or default_workspace(x.device)
+    need = workspace_bytes(w, M)
+    buf = ws.get(need)
+    cw = w.cstruct()
+    _check(lib().affqmm_run(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), buf.data_ptr() if need else None,
+                            buf.numel(), _stream_ptr(stream)), "affqmm_run")
+    return y
+
+
+def run_stacked(ws_list, x: torch.Tensor, ys=None, workspace: Workspace | None = None, stream=None):
+    """Several projections of the same x in one launch; returns a list of y."""
+    K = ws_list[0].K
+    _check_x(x, K)
+    M = x.shape[0]
+    if ys is None:
+        ys = [torch.empty(M, w.N, dtype=torch.bfloat16, device=x.device) for w in ws_list]
+    wsp = workspace or default_workspace(x.device)
+    need = workspace_bytes_stacked(ws_list, M)
+    buf = wsp.get(need)
+    arr = _warray(ws_list)
+    yp = (ctypes.c_void_p * len(ys))(*[y.data_ptr() for y in ys])
+    _check(lib().affqmm_run_stacked(len(ws_list), arr, x.data_ptr(), M, yp, buf.data_ptr() if need else None,
+                                    buf.numel(), _stream_ptr(stream)), "affqmm_run_stacked")
+    return ys
+
+
+def dequant(w: PackedWeight, stream=None) -> torch.Tensor:
+    """The bf16 [N, K] weights as the run kernels dequantize them (test hook)."""
+    out = torch.empty(w.N, w.K, dtype=torch.bfloat16, device=w.packed.device)
+    cw = w.cstruct()
+    _check(lib().affqmm_dequant(ctypes.byref(cw), out.data_ptr(), _stream_ptr(stream)), "affqmm_dequant")
+    return out
+
+
+def workspace_status(buf: torch.Tensor, stream=None) -> int:
+    """Read and clear a workspace's device status word (0 = ok)."""
+    return int(lib().affqmm_workspace_status(buf.data_ptr(), _stream_ptr(stream)))

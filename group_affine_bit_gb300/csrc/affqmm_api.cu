@@ -1,0 +1,337 @@
+// affqmm_api.cu -- the C ABI of libaffqmm: host-side validation, the work
+// decomposition and the launches.  See include/affqmm.h for the contract.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "affqmm.h"
+#include "affqmm_format.cuh"
+#include "affqmm_internal.h"
+
+using namespace affqmm;
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;   // device status word, padded
+constexpr int kMaxDevices = 64;
+constexpr size_t kSlotFloats = 256;    // one decode partial: 32 lanes x 8 floats
+
+bool valid_bits(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
+bool valid_group(int g) { return g == 32 || g == 64 || g == 128; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Per-device facts the decomposition depends on (a cache of queries, not state
+// that changes what a call computes on a given device).
+struct DeviceInfo {
+    int sms = 0;
+    int dec_occ[9][3] = {};  // [bits][mt] CTAs per SM of the decode kernel
+    bool ok = false;
+    bool is_sm103 = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+int device_info(const DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AFFQMM_E_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return AFFQMM_E_DEVICE;
+    std::call_once(g_once[dev], [dev] {
+        DeviceInfo& d = g_dev[dev];
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return;
+        d.sms = prop.multiProcessorCount;
+        d.is_sm103 = prop.major == 10 && prop.minor == 3;
+        if (!d.is_sm103) { d.ok = true; return; }
+        for (int b : {2, 3, 4, 5, 6, 8})
+            for (int mt = 1; mt <= 2; ++mt) d.dec_occ[b][mt] = std::max(1, decode_ctas_per_sm(b, mt));
+        d.ok = true;
+    });
+    const DeviceInfo& d = g_dev[dev];
+    if (!d.ok) return AFFQMM_E_CUDA;
+    if (!d.is_sm103) return AFFQMM_E_DEVICE;
+    *out = &d;
+    return AFFQMM_OK;
+}
+
+int check_weight(const affqmm_weight* w) {
+    if (!w) return AFFQMM_E_NULL;
+    if (!valid_bits(w->bits)) return AFFQMM_E_BITS;
+    if (!valid_group(w->group)) return AFFQMM_E_GROUP;
+    if (w->N < 0 || w->K < 0 || (w->K % w->group) != 0) return AFFQMM_E_SHAPE;
+    if (w->N > (int64_t)1 << 34 || w->K > (int64_t)1 << 28) return AFFQMM_E_SHAPE;
+    const int64_t tiles = (w->N + TILE_N - 1) / TILE_N;
+    const int64_t kb = (w->K + KBLK - 1) / KBLK;
+    if (tiles * kb > ((int64_t)1 << 31) - 1) return AFFQMM_E_SHAPE;
+    if (w->N > 0 && w->K > 0) {
+        if (!w->packed) return AFFQMM_E_NULL;
+        if (!aligned(w->packed, 256)) return AFFQMM_E_ALIGN;
+    }
+    return AFFQMM_OK;
+}
+
+// Depth split across CTAs for one decode projection: the smallest S whose
+// CTAs spread evenly over the SMs with enough warps resident per SM to keep
+// HBM busy.  Depends only on (tiles, k-blocks, bits, M) and the device, so a
+// projection decomposes the same way alone or inside a stacked call.
+int choose_slices(const DeviceInfo& d, int64_t tiles, int KB, int bits, int mt) {
+    const int occ = d.dec_occ[bits][mt];
+    const double sms = d.sms;
+    double best_score = -1.0;
+    int best = 1;
+    for (int S = 1; S <= 32 && S <= KB; ++S) {
+        if (S > 1 && KB < 2 * S * DEC_WARPS) break;  // at least two blocks per warp
+        const double ctas = (double)tiles * S;
+        const double per_sm = ctas / sms;
+        const double balance = per_sm / std::ceil(per_sm);
+        const double warps = std::min(per_sm, (double)occ) * DEC_WARPS;
+        const double fill = std::min(1.0, warps / 16.0);
+        const double score = balance * fill;
+        if (score > best_score * 1.01) {
+            best_score = score;
+            best = S;
+        }
+    }
+    return best;
+}
+
+struct DecodePlan {
+    DecParams p;
+    int grid = 0;
+    int mt = 1;
+    size_t ws_bytes = 0;
+};
+
+// Decomposition of a decode launch over `count` projections (M <= 16).
+int plan_decode(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan) {
+    std::memset(&plan->p, 0, sizeof(plan->p));
+    const int bits = ws[0].bits, group = ws[0].group;
+    const int64_t K = ws[0].K;
+    const int KB = (int)((K + KBLK - 1) / KBLK);
+    plan->mt = M > 8 ? 2 : 1;
+    DecParams& p = plan->p;
+    p.nproj = count;
+    p.KB = KB;
+    p.K = K;
+    p.M = (int32_t)M;
+    p.block_bytes = block_bytes(bits, group);
+    p.group = group;
+    int64_t cta = 0, ctr = 0, part = 0;
+    for (int i = 0; i < count; ++i) {
+        DecProj& P = p.proj[i];
+        P.N = ws[i].N;
+        P.packed = static_cast<const uint8_t*>(ws[i].packed);
+        const int64_t tiles = (ws[i].N + TILE_N - 1) / TILE_N;
+        P.tiles = (int32_t)tiles;
+        P.S = choose_slices(d, tiles, KB, bits, plan->mt);
+        P.cta_begin = (int32_t)cta;
+        P.ctr_begin = (int32_t)ctr;
+        P.part_begin = part;
+        cta += tiles * P.S;
+        if (P.S > 1) {
+            ctr += tiles;
+            part += tiles * P.S;
+        }
+    }
+    if (cta > ((int64_t)1 << 31) - 1) return AFFQMM_E_SHAPE;
+    plan->grid = (int)cta;
+    const size_t ctr_bytes = round_up((size_t)ctr * sizeof(uint32_t), 256);
+    plan->ws_bytes = (ctr > 0) ? kStatusBytes + ctr_bytes + (size_t)part * kSlotFloats * sizeof(float) : 0;
+    return AFFQMM_OK;
+}
+
+void bind_workspace(DecodePlan* plan, void* workspace) {
+    if (plan->ws_bytes == 0) return;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    size_t ctr = 0;
+    for (int i = 0; i < plan->p.nproj; ++i)
+        if (plan->p.proj[i].S > 1) ctr += plan->p.proj[i].tiles;
+    plan->p.counters = reinterpret_cast<uint32_t*>(base + kStatusBytes);
+    plan->p.partials = reinterpret_cast<float*>(base + kStatusBytes + round_up(ctr * sizeof(uint32_t), 256));
+}
+
+// Rows per launch: the decode kernel takes up to 16 activation rows.
+constexpr int64_t kDecodeRows = 16;
+
+int workspace_for(int count, const affqmm_weight* ws, int64_t M, size_t* bytes) {
+    const DeviceInfo* d = nullptr;
+    int rc = device_info(&d);
+    if (rc) return rc;
+    *bytes = 0;
+    if (M == 0) return AFFQMM_OK;
+    // Every launch of the call reuses the workspace; size it for the largest.
+    const int64_t full = std::min<int64_t>(M, kDecodeRows);
+    const int64_t tail = M % kDecodeRows;
+    for (int64_t mc : {full, tail}) {
+        if (mc == 0) continue;
+        DecodePlan plan;
+        rc = plan_decode(*d, count, ws, mc, &plan);
+        if (rc) return rc;
+        *bytes = std::max(*bytes, plan.ws_bytes);
+    }
+    return AFFQMM_OK;
+}
+
+int check_stack(int count, const affqmm_weight* ws) {
+    if (count < 1 || count > AFFQMM_MAX_STACK) return AFFQMM_E_ARG;
+    if (!ws) return AFFQMM_E_NULL;
+    for (int i = 0; i < count; ++i) {
+        int rc = check_weight(&ws[i]);
+        if (rc) return rc;
+        if (ws[i].K != ws[0].K || ws[i].bits != ws[0].bits || ws[i].group != ws[0].group) return AFFQMM_E_ARG;
+    }
+    return AFFQMM_OK;
+}
+
+int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, uint16_t* const* ys,
+             void* workspace, size_t ws_bytes, void* stream) {
+    int rc = check_stack(count, ws);
+    if (rc) return rc;
+    if (M < 0 || M > AFFQMM_MAX_M) return AFFQMM_E_M;
+    if (M == 0) return AFFQMM_OK;
+    const int64_t K = ws[0].K;
+    int64_t total_n = 0;
+    for (int i = 0; i < count; ++i) {
+        total_n += ws[i].N;
+        if (ws[i].N > 0 && !ys[i]) return AFFQMM_E_NULL;
+        if (ys[i] && !aligned(ys[i], 2)) return AFFQMM_E_ALIGN;
+    }
+    if (total_n == 0) return AFFQMM_OK;
+    if (K > 0) {
+        if (!x) return AFFQMM_E_NULL;
+        if (!aligned(x, 16)) return AFFQMM_E_ALIGN;
+    }
+    const DeviceInfo* d = nullptr;
+    rc = device_info(&d);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {  // an empty sum: every output is +0
+        for (int i = 0; i < count; ++i)
+            if (ws[i].N > 0 && cudaMemsetAsync(ys[i], 0, (size_t)M * ws[i].N * 2, st) != cudaSuccess)
+                return AFFQMM_E_CUDA;
+        return AFFQMM_OK;
+    }
+    size_t need = 0;
+    rc = workspace_for(count, ws, M, &need);
+    if (rc) return rc;
+    if (need > 0) {
+        if (!workspace || ws_bytes < need) return AFFQMM_E_WORKSPACE;
+        if (!aligned(workspace, 256)) return AFFQMM_E_ALIGN;
+    }
+    for (int64_t m0 = 0; m0 < M; m0 += kDecodeRows) {
+        const int64_t mc = std::min(kDecodeRows, M - m0);
+        DecodePlan plan;
+        rc = plan_decode(*d, count, ws, mc, &plan);
+        if (rc) return rc;
+        bind_workspace(&plan, workspace);
+        plan.p.x = x + m0 * K;
+        for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i] ? ys[i] + m0 * ws[i].N : nullptr;
+        if (launch_decode(ws[0].bits, plan.mt, plan.p, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
+    }
+    return AFFQMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* affqmm_strerror(int status) {
+    switch (status) {
+        case AFFQMM_OK: return "ok";
+        case AFFQMM_E_NULL: return "a required pointer is NULL";
+        case AFFQMM_E_BITS: return "bits must be 2, 3, 4, 5, 6 or 8";
+        case AFFQMM_E_GROUP: return "group must be 32, 64 or 128";
+        case AFFQMM_E_SHAPE: return "bad shape (N < 0, K < 0, K not a multiple of group, or too large)";
+        case AFFQMM_E_ALIGN: return "a pointer violates its required alignment";
+        case AFFQMM_E_M: return "M out of range";
+        case AFFQMM_E_WORKSPACE: return "workspace missing or smaller than affqmm_workspace_bytes";
+        case AFFQMM_E_TIMEOUT: return "a bounded device wait gave up";
+        case AFFQMM_E_CUDA: return "a CUDA call or launch failed";
+        case AFFQMM_E_ARG: return "bad argument (count or mismatched stacked weights)";
+        case AFFQMM_E_DEVICE: return "the current device is not an sm_103 GPU";
+        default: return "unknown affqmm status";
+    }
+}
+
+int affqmm_version(void) { return 100; }
+
+int affqmm_packed_bytes(int bits, int group, int64_t N, int64_t K, size_t* bytes) {
+    if (!bytes) return AFFQMM_E_NULL;
+    if (!valid_bits(bits)) return AFFQMM_E_BITS;
+    if (!valid_group(group)) return AFFQMM_E_GROUP;
+    if (N < 0 || K < 0 || K % group != 0 || N > (int64_t)1 << 34 || K > (int64_t)1 << 28) return AFFQMM_E_SHAPE;
+    const int64_t tiles = (N + TILE_N - 1) / TILE_N;
+    const int64_t kb = (K + KBLK - 1) / KBLK;
+    if (tiles * kb > ((int64_t)1 << 31) - 1) return AFFQMM_E_SHAPE;
+    *bytes = (size_t)tiles * (size_t)kb * (size_t)block_bytes(bits, group);
+    return AFFQMM_OK;
+}
+
+int affqmm_pack(int bits, int group, int64_t N, int64_t K, const uint8_t* codes, const uint16_t* scales,
+                const uint16_t* biases, void* packed, void* stream) {
+    size_t bytes = 0;
+    int rc = affqmm_packed_bytes(bits, group, N, K, &bytes);
+    if (rc) return rc;
+    if (bytes == 0) return AFFQMM_OK;
+    if (!packed) return AFFQMM_E_NULL;
+    if (!aligned(packed, 256)) return AFFQMM_E_ALIGN;
+    if (N > 0 && K > 0 && (!codes || !scales || !biases)) return AFFQMM_E_NULL;
+    if (launch_pack(bits, group, N, K, codes, scales, biases, packed, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return AFFQMM_E_CUDA;
+    return AFFQMM_OK;
+}
+
+int affqmm_workspace_bytes(const affqmm_weight* w, int64_t M, size_t* bytes) {
+    return affqmm_workspace_bytes_stacked(1, w, M, bytes);
+}
+
+int affqmm_workspace_bytes_stacked(int count, const affqmm_weight* ws, int64_t M, size_t* bytes) {
+    if (!bytes) return AFFQMM_E_NULL;
+    int rc = check_stack(count, ws);
+    if (rc) return rc;
+    if (M < 0 || M > AFFQMM_MAX_M) return AFFQMM_E_M;
+    return workspace_for(count, ws, M, bytes);
+}
+
+int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y, void* workspace,
+               size_t ws_bytes, void* stream) {
+    uint16_t* ys[1] = {y};
+    return run_impl(1, w, x, M, ys, workspace, ws_bytes, stream);
+}
+
+int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, uint16_t* const* ys,
+                       void* workspace, size_t ws_bytes, void* stream) {
+    if (!ys) return AFFQMM_E_NULL;
+    return run_impl(count, ws, x, M, ys, workspace, ws_bytes, stream);
+}
+
+int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* stream) {
+    int rc = check_weight(w);
+    if (rc) return rc;
+    if (w->N == 0 || w->K == 0) return AFFQMM_OK;
+    if (!w_out) return AFFQMM_E_NULL;
+    if (!aligned(w_out, 2)) return AFFQMM_E_ALIGN;
+    if (launch_dequant(w->bits, w->group, w->N, w->K, w->packed, w_out, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return AFFQMM_E_CUDA;
+    return AFFQMM_OK;
+}
+
+int affqmm_workspace_status(void* workspace, void* stream) {
+    if (!workspace) return AFFQMM_E_NULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess) return AFFQMM_E_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return AFFQMM_E_CUDA;
+    if (word == 0) return AFFQMM_OK;
+    const uint32_t zero = 0;
+    if (cudaMemcpyAsync(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice, st) != cudaSuccess) return AFFQMM_E_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return AFFQMM_E_CUDA;
+    return AFFQMM_E_TIMEOUT;
+}
+
+}  // extern "C"

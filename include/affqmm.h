@@ -1,0 +1,154 @@
+/*
+ * affqmm.h -- C ABI of libaffqmm, the GB300 (sm_103a) group-affine quantized
+ * linear projection.
+ *
+ * The operation (MLX affine tables, as used by the TensorFold pages):
+ *
+ *     W[n,k] = bf16( s[n, k/g] * q[n,k] + b[n, k/g] )      one rounding
+ *     y[m,n] = bf16( sum_k x[m,k] * W[n,k] )                fp32 accumulation
+ *
+ *   - q are integer codes of `bits` bits (2, 3, 4, 5, 6 or 8) with one bf16
+ *     scale s and one bf16 bias b per group of g = 32, 64 or 128 consecutive
+ *     k of a row: "cuda gemma4: images on the 12B" page, the embed_rows
+ *     commit ("MLX's affine tables at 2, 3, 4, 5, 6 or 8 bits (groups of 32,
+ *     64 or 128)"), and the widths commit of the same page (AffineN tiles).
+ *   - each weight is rounded once, bf16(fma(s, q, b)), and the products are
+ *     accumulated over the whole depth: "Gemma 4 12B on the native Metal
+ *     engine" page, the commit where the prompt tiles dequantize "as mlx-lm's
+ *     quantized matmul dequantizes".
+ *   - M = 1..16 activation rows (decode lanes) run a memory-bound kernel;
+ *     M >= 17 runs the tcgen05 tensor-core kernel in chunks of up to 128 rows
+ *     (prompt chunks: the same page's "128 rows in one weight read").
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device (or managed) memory of the current
+ *     device; host pointers are named as such.  All work is enqueued on
+ *     `stream` (a cudaStream_t; NULL means the legacy default stream) and is
+ *     asynchronous: the call returns once the launches are queued.
+ *   - The caller allocates and owns every buffer; the library never
+ *     allocates device memory and keeps no state between calls.
+ *   - Every argument is validated on the host before anything is launched.
+ *     A rejected call returns a nonzero affqmm_status and launches nothing.
+ *     Nothing is thrown or aborted across the ABI.
+ *   - bf16 values travel as uint16_t bit patterns.
+ */
+#ifndef AFFQMM_H
+#define AFFQMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define AFFQMM_API __attribute__((visibility("default")))
+#else
+#define AFFQMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    AFFQMM_OK = 0,
+    AFFQMM_E_NULL = 1,      /* a required pointer is NULL */
+    AFFQMM_E_BITS = 2,      /* bits not in {2,3,4,5,6,8} */
+    AFFQMM_E_GROUP = 3,     /* group not in {32,64,128} */
+    AFFQMM_E_SHAPE = 4,     /* N < 0, K < 0, K % group != 0, or sizes that overflow */
+    AFFQMM_E_ALIGN = 5,     /* a pointer violates its stated alignment */
+    AFFQMM_E_M = 6,         /* M < 0 or M > AFFQMM_MAX_M */
+    AFFQMM_E_WORKSPACE = 7, /* workspace NULL or smaller than affqmm_workspace_bytes */
+    AFFQMM_E_TIMEOUT = 8,   /* a bounded device wait gave up (see affqmm_workspace_status) */
+    AFFQMM_E_CUDA = 9,      /* a CUDA runtime call or launch failed */
+    AFFQMM_E_ARG = 10,      /* other bad argument: count, mismatched stacked weights */
+    AFFQMM_E_DEVICE = 11    /* the current device is not an sm_103 GPU */
+} affqmm_status;
+
+/* Largest M one call accepts (larger batches: split them). */
+#define AFFQMM_MAX_M (1 << 20)
+/* Most projections one affqmm_run_stacked call takes. */
+#define AFFQMM_MAX_STACK 8
+
+/* A packed weight: a non-owning view of memory filled by affqmm_pack.
+ * `packed` is device memory of affqmm_packed_bytes(bits, group, N, K) bytes,
+ * 256-byte aligned.  Its layout is private to this library and may change
+ * between versions; only affqmm_pack writes it. */
+typedef struct {
+    int32_t bits;
+    int32_t group;
+    int64_t N;
+    int64_t K;
+    const void* packed;
+} affqmm_weight;
+
+/* A static string naming a status code (never NULL). */
+AFFQMM_API const char* affqmm_strerror(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+AFFQMM_API int affqmm_version(void);
+
+/* Bytes of packed storage for an N x K table (host call, no GPU needed).
+ * Rows are padded to multiples of 16 and the depth to multiples of 128; the
+ * padding holds zero codes with zero scale and bias.
+ * Errors: E_NULL (bytes), E_BITS, E_GROUP, E_SHAPE. */
+AFFQMM_API int affqmm_packed_bytes(int bits, int group, int64_t N, int64_t K, size_t* bytes);
+
+/* Pack a canonical affine table into the library's layout.
+ *   codes   device, uint8 [N, K] row-major, one code per byte; bits above
+ *           `bits` are ignored (a code is taken modulo 2^bits)
+ *   scales  device, bf16 [N, K/group] row-major
+ *   biases  device, bf16 [N, K/group] row-major
+ *   packed  device, affqmm_packed_bytes() bytes, 256-byte aligned, written
+ * The same table as MLX's affine quantization stores it (scale and bias per
+ * group along a row), unpacked to one code per byte.
+ * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_CUDA. */
+AFFQMM_API int affqmm_pack(int bits, int group, int64_t N, int64_t K,
+                const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
+                void* packed, void* stream);
+
+/* Bytes of workspace that affqmm_run needs for this weight and M on the
+ * current device (split-K partial sums, merge counters and a status word).
+ * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_M, E_DEVICE, E_CUDA. */
+AFFQMM_API int affqmm_workspace_bytes(const affqmm_weight* w, int64_t M, size_t* bytes);
+
+/* The same for a stacked call over `count` weights. */
+AFFQMM_API int affqmm_workspace_bytes_stacked(int count, const affqmm_weight* ws, int64_t M,
+                                   size_t* bytes);
+
+/* y = bf16(x . W^T), fp32 accumulation, the weights dequantized on the fly.
+ *   w          host pointer to the weight view (its `packed` is device memory)
+ *   x          device, bf16 [M, K] row-major, 16-byte aligned
+ *   y          device, bf16 [M, N] row-major, 2-byte aligned; fully written
+ *   workspace  device, >= affqmm_workspace_bytes bytes, 256-byte aligned,
+ *              ZERO-FILLED before its first use; every call leaves it in that
+ *              state again.  May be NULL when the required size is 0.
+ *              Calls that share a workspace must not overlap on the GPU.
+ * M = 0 or N = 0 launches nothing; K = 0 writes zeros.
+ * The result is deterministic: the same inputs give the same bits.
+ * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_M, E_WORKSPACE,
+ *         E_DEVICE, E_CUDA. */
+AFFQMM_API int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y,
+               void* workspace, size_t ws_bytes, void* stream);
+
+/* Several projections of the same x in one launch (q/k/v, gate/up stacks).
+ *   ws      host array of `count` weight views (1 <= count <= AFFQMM_MAX_STACK)
+ *           with equal K, bits and group
+ *   ys      host array of `count` device pointers, ys[i] is bf16 [M, ws[i].N]
+ * Each ys[i] equals affqmm_run(&ws[i], x, ...) bit for bit.
+ * Errors: as affqmm_run, plus E_ARG for a bad count or mismatched weights. */
+AFFQMM_API int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M,
+                       uint16_t* const* ys, void* workspace, size_t ws_bytes, void* stream);
+
+/* Test hook: write the dequantized weights W (bf16 [N, K] row-major, device,
+ * 2-byte aligned) with the same device arithmetic the run kernels use.
+ * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_CUDA. */
+AFFQMM_API int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* stream);
+
+/* Read and clear the device status word of a workspace (synchronizes
+ * `stream`).  Returns AFFQMM_OK, or AFFQMM_E_TIMEOUT when a kernel that used
+ * this workspace gave up a bounded wait (its outputs are then invalid). */
+AFFQMM_API int affqmm_workspace_status(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
