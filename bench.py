@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark of the group-affine quantized projection (libaffqmm) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  A step is one pass of the projection path
+over one batch of synthetic input with the weights resident in HBM:
+
+  gate_up_decode (default)  M=1, K=3840, N=30720 (stacked gate/up), 4-bit g64
+  decode_step               a 60-layer decoder's projections + tied head, M=1
+  prompt_chunk              M=128 through one layer's four projection shapes
+  lane_sweep                M in {2,4,8,16} at 4-bit g64 and M=16 at 8b/3b/2b
+  tiny                      M=1, K=256, N=512, 4-bit g64
+
+`value` is packed-weight bytes (codes + bf16 scales + biases) per second for
+the decode workloads and TFLOP/s for the prompt chunk.  Weight copies rotate
+so that the bytes touched between two reads of one copy exceed the 129 MB L2.
+Steps are replayed from CUDA graphs and timed with CUDA events on the stream
+that launches them.  `e2e` times the same steps through the Python API with
+the activations uploaded from pinned host memory and the outputs read back
+every step.  `--impl reference` times the CPU oracle on a bounded sample of
+the same workload on the host cores.  Under torchrun every rank runs an
+independent replica (the path needs no exchange) and rank 0 reports the
+aggregate over ranks with the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "affine-4bit qmm packed-weight GB/s vs HBM peak (M=1..16); TFLOP/s at M=128"
+L2_BYTES = 129 * 10 ** 6
+KERNEL_SOURCES = ["group_affine_bit_gb300/csrc/decode.cu", "group_affine_bit_gb300/csrc/affqmm_format.cuh",
+                  "group_affine_bit_gb300/csrc/prompt.cu"]
+
+
+# ----------------------------------------------------------------------------- setup
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="gate_up_decode",
+                    choices=["gate_up_decode", "decode_step", "prompt_chunk", "lane_sweep", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_max(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def aggregate(per_rank_units: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank processed the same units."""
+    return per_rank_units * world / max_seconds
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        p = os.path.join(ROOT, rel)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def committed_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(key)
+    if not d or d.get("src_digest") != source_digest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the GPU is busy."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[2]), smax=float(parts[3]), power=float(parts[4]),
+                                 hw=parts[6], hwth=parts[7], swth=parts[8], swpc=parts[9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r["power"] > 0.3 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwth", "hw_thermal_slowdown"),
+                              ("swth", "sw_thermal_slowdown"), ("swpc", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ----------------------------------------------------------------------------- workloads
+class Projection:
+    """One resident projection with `copies` rotating weight copies."""
+
+    def __init__(self, api, synth, bits, group, M, N, K, seed, copies, device):
+        import torch
+        self.bits, self.group, self.M, self.N, self.K = bits, group, M, N, K
+        g = synth.generator(seed, device)
+        self.ws = []
+        for _ in range(copies):
+            codes, s, b = synth.affine_table(bits, group, N, K, g, device)
+            self.ws.append(api.pack(codes, s, b, bits, group))
+            del codes, s, b
+        self.x = synth.activations(M, K, g, device)
+        self.y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+
+    @property
+    def packed_bytes(self) -> int:
+        return self.N * self.K * self.bits // 8 + 4 * self.N * self.K // self.group
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        return self.packed_bytes + 2 * self.M * self.K + 2 * self.M * self.N
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+def copies_for(bytes_per_copy: int) -> int:
+    return max(4, math.ceil(2 * L2_BYTES / max(1, bytes_per_copy)))
+
+
+class GateUpDecode:
+    name = "gate_up_decode"
+    unit = "GB/s"
+
+    def __init__(self, api, synth, device, shape=None):
+        c = shape or synth.GATE_UP_DECODE
+        self.cfg = dict(c)
+        one = c["N"] * c["K"] * c["bits"] // 8 + 4 * c["N"] * c["K"] // c["group"]
+        self.copies = copies_for(one)
+        self.p = Projection(api, synth, c["bits"], c["group"], c["M"], c["N"], c["K"], c["seed"], self.copies, device)
+        self.api = api
+        self.ws = api.Workspace(device)
+
+    def step(self, i: int):
+        self.api.run(self.p.ws[i % self.copies], self.p.x, y=self.p.y, workspace=self.ws)
+
+    launches_per_step = 1
+    units_per_step = property(lambda self: self.p.packed_bytes)
+
+    def roofline_info(self):
+        return dict(kernel=f"decode_kernel<{self.p.bits},{1 if self.p.M <= 8 else 2}>", bound="hbm",
+                    units_per_launch=self.p.algorithmic_bytes, launches_per_step=1,
+                    traffic_key=f"decode {self.name} M{self.p.M}")
+
+    def config(self):
+        c = self.cfg
+        return {"workload": f"{self.name}: M={c['M']} K={c['K']} N={c['N']} {c['bits']}-bit group {c['group']}",
+                "M": c["M"], "K": c["K"], "N": c["N"], "bits": c["bits"], "group": c["group"], "seed": c["seed"],
+                "l2": f"inputs larger than L2: {self.copies} rotating weight copies "
+                      f"({self.copies * self.p.packed_bytes / 1e6:.0f} MB > 129 MB L2)",
+                "parallelism": "replicas"}
+
+    # host-side I/O of one step for the end-to-end timing
+    def e2e_io(self):
+        return [self.p.x], [self.p.y]
+
+    def oracle_problem(self):
+        return [(self.cfg["bits"], self.cfg["group"], self.cfg["M"], self.cfg["N"], self.cfg["K"], self.cfg["seed"])]
+
+
+class Tiny(GateUpDecode):
+    name = "tiny"
+
+    def __init__(self, api, synth, device):
+        super().__init__(api, synth, device, synth.TINY)
+
+
+WORKLOADS = {"gate_up_decode": GateUpDecode, "tiny": Tiny}
+
+
+# ----------------------------------------------------------------------------- timing
+def graph_of(fn, first: int, count: int):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(first, first + count):
+            fn(i)
+    return g
+
+
+def time_steps(wl, steps: int, warmup: int, dist, device):
+    """Device time of exactly `steps` steps replayed from CUDA graphs."""
+    import torch
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        for i in range(warmup):       # eager warm-up (also initializes the library)
+            wl.step(i)
+    torch.cuda.current_stream(device).wait_stream(side)
+    torch.cuda.synchronize(device)
+    chunk = min(steps, 500)
+    full = graph_of(wl.step, 0, chunk)
+    rest = graph_of(wl.step, 0, steps % chunk) if steps % chunk else None
+    for _ in range(max(1, warmup // chunk)):
+        full.replay()
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(steps // chunk):
+        full.replay()
+    if rest is not None:
+        rest.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    seconds = e0.elapsed_time(e1) * 1e-3
+    return seconds, (full, rest, chunk)
+
+
+def sustain_for_clocks(graphs, device, seconds: float = 1.0):
+    """Replay the timed graphs for about `seconds` so the clock sampler sees
+    the same load when the timed region itself is too short to sample."""
+    import torch
+    full, rest, chunk = graphs
+    t0 = time.time()
+    while time.time() - t0 < seconds:
+        full.replay()
+        torch.cuda.synchronize(device)
+
+
+def time_e2e(wl, api, steps: int, device):
+    """Same steps through the Python API, activations uploaded from pinned host
+    memory and outputs read back to pinned host memory every step."""
+    import torch
+    ins, outs = wl.e2e_io()
+    h_in = [t.detach().cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    bi = sum(t.numel() * t.element_size() for t in h_in)
+    bo = sum(t.numel() * t.element_size() for t in h_out)
+    stream = torch.cuda.current_stream(device)
+    for i in range(3):
+        wl.step(i)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(steps):
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        wl.step(i)
+        for d, h in zip(outs, h_out):
+            h.copy_(d, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t0
+    return max(wall, e0.elapsed_time(e1) * 1e-3), bi, bo
+
+
+# ----------------------------------------------------------------------------- oracle
+class OracleSample:
+    """The CPU oracle on a bounded sample of a workload: whole output rows of
+    the same projection (same seed, same values), threaded over rows on all
+    host cores.  Rate = packed-weight bytes of the sampled rows per second."""
+
+    def __init__(self, wl_name: str):
+        import oracle
+        from group_affine_bit_gb300 import synth
+        self.orc = oracle.load()
+        shape = synth.TINY if wl_name == "tiny" else synth.GATE_UP_DECODE
+        self.bits, self.group = shape["bits"], shape["group"]
+        self.M, self.N, self.K = shape["M"], shape["N"], shape["K"]
+        x, codes, s, b = synth.problem(self.bits, self.group, self.M, self.N, self.K, shape["seed"])
+        self.xb, self.cb = synth.bits_u16(x), codes.numpy()
+        self.sb, self.bb = synth.bits_u16(s), synth.bits_u16(b)
+        self.threads = host_cores()
+
+    def row_bytes(self, rows: int) -> int:
+        return rows * self.K * self.bits // 8 + 4 * rows * self.K // self.group
+
+    def run(self, rows: int) -> float:
+        t0 = time.perf_counter()
+        self.orc.qmm(self.bits, self.group, self.xb, self.cb[:rows], self.sb[:rows], self.bb[:rows],
+                     nthreads=self.threads)
+        return time.perf_counter() - t0
+
+    def rows_for(self, seconds: float) -> int:
+        n = min(self.N, 64)
+        dt = max(self.run(n), 1e-5)
+        return int(max(1, min(self.N, n * seconds / dt)))
+
+    def describe(self, rows: int, reps: int) -> str:
+        return (f"{reps} x {rows} of {self.N} output rows of the same projection (M={self.M}, K={self.K}, "
+                f"{self.bits}-bit g{self.group}); float64 oracle threaded over rows")
+
+    def rate(self, seconds: float):
+        rows = self.rows_for(seconds)
+        reps, total = 0, 0.0
+        while total < seconds or reps == 0:
+            total += self.run(rows)
+            reps += 1
+        return self.row_bytes(rows) * reps / total / 1e9, self.describe(rows, reps), total
+
+
+# ----------------------------------------------------------------------------- main
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: rank 0 only; each step is one
+    bounded sample of the workload."""
+    if rank != 0:
+        return 0
+    smp = OracleSample(args.workload)
+    per_step = max(0.02, args.cpu_seconds / max(1, args.steps + args.warmup))
+    rows = smp.rows_for(per_step)
+    for _ in range(args.warmup):
+        smp.run(rows)
+    total = 0.0
+    for _ in range(args.steps):
+        total += smp.run(rows)
+    value = smp.row_bytes(rows) * args.steps / total / 1e9
+    sample = smp.describe(rows, 1) + " per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / max(1, args.steps) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": smp.threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    from group_affine_bit_gb300 import api, build, synth
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    if rank == 0:
+        build.build()
+    barrier(dist)
+    api.lib()
+
+    wl = WORKLOADS[args.workload](api, synth, device)
+    warmup = max(3, args.warmup)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    seconds, graphs = time_steps(wl, args.steps, warmup, dist, device)
+    if sampler:
+        if seconds < 1.0:
+            sustain_for_clocks(graphs, device, 1.0)
+        clocks = sampler.stop()
+    t_max = reduce_max(dist, seconds, device)
+    units = wl.units_per_step * args.steps
+    value = aggregate(units, world, t_max) / 1e9
+
+    info = wl.roofline_info()
+    peaks = measured_peaks()
+    achieved = info["units_per_launch"] / (seconds / (args.steps * info["launches_per_step"])) / 1e9
+    roofline = {"bound": info["bound"], "kernel": info["kernel"], "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_source": f"{peaks['source']} hbm_gbs (copy)",
+                "traffic": committed_traffic(info["traffic_key"]),
+                "bytes_per_launch": info["units_per_launch"]}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = min(args.steps, 2000)
+        t_e2e, bi, bo = time_e2e(wl, api, e2e_steps, device)
+        t_e2e = reduce_max(dist, t_e2e, device)
+        e2e = {"value": aggregate(wl.units_per_step * e2e_steps, world, t_e2e) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = OracleSample(args.workload)
+        r, sample, dt = smp.rate(args.cpu_seconds)
+        cpu = {"value": r, "unit": "GB/s", "cores": smp.threads, "kind": "oracle", "sample": sample,
+               "seconds": round(dt, 2)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": wl.config(), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps * wl.launches_per_step, "clocks": clocks,
+                "kernel_src_digest": source_digest()}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
