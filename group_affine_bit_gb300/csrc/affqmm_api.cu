@@ -26,12 +26,35 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Per-device facts the decomposition depends on (a cache of queries, not state
 // that changes what a call computes on a given device).
+struct RingCfg {
+    int stages = 0;       // shared-memory stages per warp
+    int stage_bytes = 0;  // stage stride
+    int ctas = 0;         // resident CTAs per SM with that ring
+};
+
+int group_index(int g) { return g == 32 ? 0 : g == 64 ? 1 : 2; }
+
 struct DeviceInfo {
     int sms = 0;
-    int dec_occ[9][3] = {};  // [bits][mt] CTAs per SM of the decode kernel
+    RingCfg ring[9][3][3];  // decode kernel ring by [bits][group index][mt]
     bool ok = false;
     bool is_sm103 = false;
 };
+
+// The decode ring: as many stages per warp as fit in about 200 KB of shared
+// memory per SM at the occupancy the kernel's registers allow.
+RingCfg make_ring(int bits, int group, int mt) {
+    RingCfg c;
+    c.stage_bytes = (int)round_up((size_t)block_bytes(bits, group), 128);
+    const int by_regs = std::max(1, decode_ctas_per_sm(bits, mt, 0));
+    const size_t budget = 200 * 1024;
+    int ns = (int)(budget / ((size_t)by_regs * DEC_WARPS * (c.stage_bytes + 8)));
+    ns = std::max(2, std::min(ns, 16));
+    while (ns > 2 && decode_smem_bytes(ns, c.stage_bytes) > (size_t)kDecodeSmemMax) --ns;
+    c.stages = ns;
+    c.ctas = std::max(1, decode_ctas_per_sm(bits, mt, decode_smem_bytes(ns, c.stage_bytes)));
+    return c;
+}
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_once[kMaxDevices];
 
@@ -46,8 +69,10 @@ int device_info(const DeviceInfo** out) {
         d.sms = prop.multiProcessorCount;
         d.is_sm103 = prop.major == 10 && prop.minor == 3;
         if (!d.is_sm103) { d.ok = true; return; }
+        if (decode_allow_smem(kDecodeSmemMax) != cudaSuccess) return;
         for (int b : {2, 3, 4, 5, 6, 8})
-            for (int mt = 1; mt <= 2; ++mt) d.dec_occ[b][mt] = std::max(1, decode_ctas_per_sm(b, mt));
+            for (int g : {32, 64, 128})
+                for (int mt = 1; mt <= 2; ++mt) d.ring[b][group_index(g)][mt] = make_ring(b, g, mt);
         d.ok = true;
     });
     const DeviceInfo& d = g_dev[dev];
@@ -73,39 +98,19 @@ int check_weight(const affqmm_weight* w) {
     return AFFQMM_OK;
 }
 
-// Depth split across CTAs for one decode projection: the smallest S whose
-// CTAs spread evenly over the SMs with enough warps resident per SM to keep
-// HBM busy.  Depends only on (tiles, k-blocks, bits, M) and the device, so a
-// projection decomposes the same way alone or inside a stacked call.
-int choose_slices(const DeviceInfo& d, int64_t tiles, int KB, int bits, int mt) {
-    const int occ = d.dec_occ[bits][mt];
-    const double sms = d.sms;
-    double best_score = -1.0;
-    int best = 1;
-    for (int S = 1; S <= 32 && S <= KB; ++S) {
-        if (S > 1 && KB < 2 * S * DEC_WARPS) break;  // at least two blocks per warp
-        const double ctas = (double)tiles * S;
-        const double per_sm = ctas / sms;
-        const double balance = per_sm / std::ceil(per_sm);
-        const double warps = std::min(per_sm, (double)occ) * DEC_WARPS;
-        const double fill = std::min(1.0, warps / 16.0);
-        const double score = balance * fill;
-        if (score > best_score * 1.01) {
-            best_score = score;
-            best = S;
-        }
-    }
-    return best;
-}
-
 struct DecodePlan {
     DecParams p;
     int grid = 0;
     int mt = 1;
     size_t ws_bytes = 0;
+    size_t ctr_bytes = 0;
+    size_t smem = 0;
 };
 
-// Decomposition of a decode launch over `count` projections (M <= 16).
+// Decomposition of a decode launch over `count` projections (M <= 16): each
+// projection's blocks are cut into as many contiguous runs as the device
+// holds resident warps of the kernel (fewer if it has fewer blocks).  The cut
+// of one projection does not depend on the others in the launch.
 int plan_decode(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan) {
     std::memset(&plan->p, 0, sizeof(plan->p));
     const int bits = ws[0].bits, group = ws[0].group;
@@ -119,38 +124,41 @@ int plan_decode(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t
     p.M = (int32_t)M;
     p.block_bytes = block_bytes(bits, group);
     p.group = group;
-    int64_t cta = 0, ctr = 0, part = 0;
+    const RingCfg& ring = d.ring[bits][group_index(group)][plan->mt];
+    p.stages = ring.stages;
+    p.stage_bytes = ring.stage_bytes;
+    plan->smem = decode_smem_bytes(ring.stages, ring.stage_bytes);
+    const int64_t resident = (int64_t)d.sms * ring.ctas * DEC_WARPS;
+    int64_t warps = 0, tiles_total = 0;
     for (int i = 0; i < count; ++i) {
         DecProj& P = p.proj[i];
         P.N = ws[i].N;
         P.packed = static_cast<const uint8_t*>(ws[i].packed);
         const int64_t tiles = (ws[i].N + TILE_N - 1) / TILE_N;
+        const int64_t units = tiles * KB;
         P.tiles = (int32_t)tiles;
-        P.S = choose_slices(d, tiles, KB, bits, plan->mt);
-        P.cta_begin = (int32_t)cta;
-        P.ctr_begin = (int32_t)ctr;
-        P.part_begin = part;
-        cta += tiles * P.S;
-        if (P.S > 1) {
-            ctr += tiles;
-            part += tiles * P.S;
-        }
+        P.units = (int32_t)units;
+        P.nwarps = (int32_t)std::min<int64_t>(resident, units);
+        P.warp_begin = (int32_t)warps;
+        P.ctr_begin = (int32_t)tiles_total;
+        P.slot_begin = (int32_t)(2 * warps);
+        warps += P.nwarps;
+        tiles_total += tiles;
     }
-    if (cta > ((int64_t)1 << 31) - 1) return AFFQMM_E_SHAPE;
-    plan->grid = (int)cta;
-    const size_t ctr_bytes = round_up((size_t)ctr * sizeof(uint32_t), 256);
-    plan->ws_bytes = (ctr > 0) ? kStatusBytes + ctr_bytes + (size_t)part * kSlotFloats * sizeof(float) : 0;
+    if (warps > ((int64_t)1 << 30)) return AFFQMM_E_SHAPE;
+    p.total_warps = (int32_t)warps;
+    plan->grid = (int)((warps + DEC_WARPS - 1) / DEC_WARPS);
+    plan->ctr_bytes = round_up((size_t)tiles_total * sizeof(uint32_t), 256);
+    plan->ws_bytes = warps > 0 ? kStatusBytes + plan->ctr_bytes + (size_t)(2 * warps) * kSlotFloats * sizeof(float) : 0;
     return AFFQMM_OK;
 }
 
 void bind_workspace(DecodePlan* plan, void* workspace) {
     if (plan->ws_bytes == 0) return;
     uint8_t* base = static_cast<uint8_t*>(workspace);
-    size_t ctr = 0;
-    for (int i = 0; i < plan->p.nproj; ++i)
-        if (plan->p.proj[i].S > 1) ctr += plan->p.proj[i].tiles;
+    plan->p.status = reinterpret_cast<uint32_t*>(base);
     plan->p.counters = reinterpret_cast<uint32_t*>(base + kStatusBytes);
-    plan->p.partials = reinterpret_cast<float*>(base + kStatusBytes + round_up(ctr * sizeof(uint32_t), 256));
+    plan->p.partials = reinterpret_cast<float*>(base + kStatusBytes + plan->ctr_bytes);
 }
 
 // Rows per launch: the decode kernel takes up to 16 activation rows.

@@ -176,6 +176,36 @@ __device__ __forceinline__ void load_lane_codes(const uint8_t* blk, int lane, ui
     }
 }
 
+// The same lane words read from a block staged in shared memory (same layout).
+template <int BITS>
+__device__ __forceinline__ void load_lane_codes_smem(uint32_t blk, int lane, uint32_t* cw) {
+    constexpr int P0 = plane0_bits(BITS);
+    constexpr int P1 = plane1_bits(BITS);
+#pragma unroll
+    for (int c = 0; c < lane_plane_bytes(P0) / chunk_bytes(P0); ++c) {
+        const uint32_t a = blk + plane_offset(BITS, 0) + c * 32 * chunk_bytes(P0) + lane * chunk_bytes(P0);
+        if constexpr (chunk_bytes(P0) == 16)
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(cw[4 * c]), "=r"(cw[4 * c + 1]), "=r"(cw[4 * c + 2]), "=r"(cw[4 * c + 3])
+                         : "r"(a));
+        else
+            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(cw[2 * c]), "=r"(cw[2 * c + 1]) : "r"(a));
+    }
+    if constexpr (P1 > 0) {
+#pragma unroll
+        for (int c = 0; c < lane_plane_bytes(P1) / chunk_bytes(P1); ++c) {
+            const uint32_t a = blk + plane_offset(BITS, 1) + c * 32 * chunk_bytes(P1) + lane * chunk_bytes(P1);
+            uint32_t* d = cw + 2 * P0;
+            if constexpr (chunk_bytes(P1) == 16)
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(d[4 * c]), "=r"(d[4 * c + 1]), "=r"(d[4 * c + 2]), "=r"(d[4 * c + 3])
+                             : "r"(a));
+            else
+                asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(d[2 * c]), "=r"(d[2 * c + 1]) : "r"(a));
+        }
+    }
+}
+
 #endif  // __CUDACC__
 
 }  // namespace affqmm
