@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libaffqmm.so")
 
 MAX_STACK = 8
 MAX_M = 1 << 20
+WORKSPACE_ZEROED = 256 + 65536 * 4   # leading workspace bytes kept zero between calls
 
 STATUS_NAMES = {
     0: "AFFQMM_OK", 1: "AFFQMM_E_NULL", 2: "AFFQMM_E_BITS", 3: "AFFQMM_E_GROUP",

@@ -1,5 +1,6 @@
 // affqmm_api.cu -- the C ABI of libaffqmm: host-side validation, the work
 // decomposition and the launches.  See include/affqmm.h for the contract.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -15,7 +16,6 @@ using namespace affqmm;
 
 namespace {
 
-constexpr size_t kStatusBytes = 256;   // device status word, padded
 constexpr int kMaxDevices = 64;
 constexpr size_t kSlotFloats = 256;    // one decode partial: 32 lanes x 8 floats
 
@@ -70,6 +70,7 @@ int device_info(const DeviceInfo** out) {
         d.is_sm103 = prop.major == 10 && prop.minor == 3;
         if (!d.is_sm103) { d.ok = true; return; }
         if (decode_allow_smem(kDecodeSmemMax) != cudaSuccess) return;
+        if (prompt_allow_smem() != cudaSuccess) return;
         for (int b : {2, 3, 4, 5, 6, 8})
             for (int g : {32, 64, 128})
                 for (int mt = 1; mt <= 2; ++mt) d.ring[b][group_index(g)][mt] = make_ring(b, g, mt);
@@ -103,7 +104,6 @@ struct DecodePlan {
     int grid = 0;
     int mt = 1;
     size_t ws_bytes = 0;
-    size_t ctr_bytes = 0;
     size_t smem = 0;
 };
 
@@ -146,10 +146,10 @@ int plan_decode(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t
         tiles_total += tiles;
     }
     if (warps > ((int64_t)1 << 30)) return AFFQMM_E_SHAPE;
+    if (tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
     p.total_warps = (int32_t)warps;
     plan->grid = (int)((warps + DEC_WARPS - 1) / DEC_WARPS);
-    plan->ctr_bytes = round_up((size_t)tiles_total * sizeof(uint32_t), 256);
-    plan->ws_bytes = warps > 0 ? kStatusBytes + plan->ctr_bytes + (size_t)(2 * warps) * kSlotFloats * sizeof(float) : 0;
+    plan->ws_bytes = warps > 0 ? kSlotsOffset + (size_t)(2 * warps) * kSlotFloats * sizeof(float) : 0;
     return AFFQMM_OK;
 }
 
@@ -158,11 +158,89 @@ void bind_workspace(DecodePlan* plan, void* workspace) {
     uint8_t* base = static_cast<uint8_t*>(workspace);
     plan->p.status = reinterpret_cast<uint32_t*>(base);
     plan->p.counters = reinterpret_cast<uint32_t*>(base + kStatusBytes);
-    plan->p.partials = reinterpret_cast<float*>(base + kStatusBytes + plan->ctr_bytes);
+    plan->p.partials = reinterpret_cast<float*>(base + kSlotsOffset);
 }
 
-// Rows per launch: the decode kernel takes up to 16 activation rows.
+// Rows per launch: the decode kernel takes up to 16 activation rows, the
+// prompt kernel up to 128.
 constexpr int64_t kDecodeRows = 16;
+constexpr int64_t kPromptRows = 128;
+constexpr int kPromptTileN = 256;
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiledFn) nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// x [M, K] bf16 row-major as 64 (k) x 128 (rows) boxes with the 128-byte
+// swizzle the tensor core reads; rows past M and k past K read as zero.
+int make_x_map(const uint16_t* x, int64_t M, int64_t K, CUtensorMap* map) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return AFFQMM_E_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? AFFQMM_OK : AFFQMM_E_CUDA;
+}
+
+struct PromptPlan {
+    PromptParams p;
+    int grid = 0;
+    size_t ws_bytes = 0;
+};
+
+// Decomposition of a prompt launch: each projection's (256-row tile, block)
+// units are cut into one run per SM (fewer if it has fewer units).
+int plan_prompt(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, PromptPlan* plan) {
+    std::memset(&plan->p, 0, sizeof(plan->p));
+    PromptParams& p = plan->p;
+    const int bits = ws[0].bits, group = ws[0].group;
+    const int64_t K = ws[0].K;
+    const int KB = (int)((K + KBLK - 1) / KBLK);
+    p.nproj = count;
+    p.KB = KB;
+    p.K = K;
+    p.M = (int32_t)M;
+    p.block_bytes = block_bytes(bits, group);
+    p.group = group;
+    int64_t ctas = 0, tiles_total = 0;
+    for (int i = 0; i < count; ++i) {
+        PromptProj& P = p.proj[i];
+        P.N = ws[i].N;
+        P.packed = static_cast<const uint8_t*>(ws[i].packed);
+        P.tiles16 = (int32_t)((ws[i].N + TILE_N - 1) / TILE_N);
+        const int64_t tiles = (ws[i].N + kPromptTileN - 1) / kPromptTileN;
+        P.tiles = (int32_t)tiles;
+        P.units = (int32_t)(tiles * KB);
+        P.nctas = (int32_t)std::min<int64_t>(d.sms, P.units);
+        P.cta_begin = (int32_t)ctas;
+        P.ctr_begin = (int32_t)tiles_total;
+        P.slot_begin = (int32_t)(2 * ctas);
+        ctas += P.nctas;
+        tiles_total += tiles;
+    }
+    if (4 * tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
+    plan->grid = (int)ctas;
+    plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kPromptSlotFloats * sizeof(float) : 0;
+    return AFFQMM_OK;
+}
 
 int workspace_for(int count, const affqmm_weight* ws, int64_t M, size_t* bytes) {
     const DeviceInfo* d = nullptr;
@@ -170,15 +248,16 @@ int workspace_for(int count, const affqmm_weight* ws, int64_t M, size_t* bytes) 
     if (rc) return rc;
     *bytes = 0;
     if (M == 0) return AFFQMM_OK;
-    // Every launch of the call reuses the workspace; size it for the largest.
-    const int64_t full = std::min<int64_t>(M, kDecodeRows);
-    const int64_t tail = M % kDecodeRows;
-    for (int64_t mc : {full, tail}) {
-        if (mc == 0) continue;
+    if (M <= kDecodeRows) {
         DecodePlan plan;
-        rc = plan_decode(*d, count, ws, mc, &plan);
+        rc = plan_decode(*d, count, ws, M, &plan);
         if (rc) return rc;
-        *bytes = std::max(*bytes, plan.ws_bytes);
+        *bytes = plan.ws_bytes;
+    } else {
+        PromptPlan plan;
+        rc = plan_prompt(*d, count, ws, std::min<int64_t>(M, kPromptRows), &plan);
+        if (rc) return rc;
+        *bytes = plan.ws_bytes;
     }
     return AFFQMM_OK;
 }
@@ -229,15 +308,31 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         if (!workspace || ws_bytes < need) return AFFQMM_E_WORKSPACE;
         if (!aligned(workspace, 256)) return AFFQMM_E_ALIGN;
     }
-    for (int64_t m0 = 0; m0 < M; m0 += kDecodeRows) {
-        const int64_t mc = std::min(kDecodeRows, M - m0);
+    if (M <= kDecodeRows) {
         DecodePlan plan;
-        rc = plan_decode(*d, count, ws, mc, &plan);
+        rc = plan_decode(*d, count, ws, M, &plan);
         if (rc) return rc;
         bind_workspace(&plan, workspace);
-        plan.p.x = x + m0 * K;
-        for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i] ? ys[i] + m0 * ws[i].N : nullptr;
+        plan.p.x = x;
+        for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i];
         if (launch_decode(ws[0].bits, plan.mt, plan.p, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
+        return AFFQMM_OK;
+    }
+    // Prompt rows: chunks of up to 128 rows on the tensor-core kernel.
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    for (int64_t m0 = 0; m0 < M; m0 += kPromptRows) {
+        const int64_t mc = std::min(kPromptRows, M - m0);
+        PromptPlan plan;
+        rc = plan_prompt(*d, count, ws, mc, &plan);
+        if (rc) return rc;
+        plan.p.status = reinterpret_cast<uint32_t*>(wsb);
+        plan.p.counters = reinterpret_cast<uint32_t*>(wsb + kStatusBytes);
+        plan.p.slots = reinterpret_cast<float*>(wsb + kSlotsOffset);
+        for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i] ? ys[i] + m0 * ws[i].N : nullptr;
+        CUtensorMap map;
+        rc = make_x_map(x + m0 * K, mc, K, &map);
+        if (rc) return rc;
+        if (launch_prompt(ws[0].bits, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
     }
     return AFFQMM_OK;
 }

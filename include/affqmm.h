@@ -67,6 +67,8 @@ typedef enum {
 #define AFFQMM_MAX_M (1 << 20)
 /* Most projections one affqmm_run_stacked call takes. */
 #define AFFQMM_MAX_STACK 8
+/* Leading workspace bytes that must be zero between calls (status + counters). */
+#define AFFQMM_WORKSPACE_ZEROED (256 + 65536 * 4)
 
 /* A packed weight: a non-owning view of memory filled by affqmm_pack.
  * `packed` is device memory of affqmm_packed_bytes(bits, group, N, K) bytes,
@@ -118,10 +120,13 @@ AFFQMM_API int affqmm_workspace_bytes_stacked(int count, const affqmm_weight* ws
  *   w          host pointer to the weight view (its `packed` is device memory)
  *   x          device, bf16 [M, K] row-major, 16-byte aligned
  *   y          device, bf16 [M, N] row-major, 2-byte aligned; fully written
- *   workspace  device, >= affqmm_workspace_bytes bytes, 256-byte aligned,
- *              ZERO-FILLED before its first use; every call leaves it in that
- *              state again.  May be NULL when the required size is 0.
- *              Calls that share a workspace must not overlap on the GPU.
+ *   workspace  device, >= affqmm_workspace_bytes bytes, 256-byte aligned.
+ *              Its first AFFQMM_WORKSPACE_ZEROED bytes (a status word and the
+ *              merge counters) must be zero before its first use; every call
+ *              that returns AFFQMM_OK leaves them zero again, the rest is
+ *              scratch.  May be NULL when the required size is 0.  Calls that
+ *              share a workspace must not overlap on the GPU.  After a call
+ *              reported AFFQMM_E_TIMEOUT, zero that prefix again.
  * M = 0 or N = 0 launches nothing; K = 0 writes zeros.
  * The result is deterministic: the same inputs give the same bits.
  * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_M, E_WORKSPACE,
