@@ -27,7 +27,7 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Per-device facts the decomposition depends on (a cache of queries, not state
 // that changes what a call computes on a given device).
 struct RingCfg {
-    int stages = 0;       // shared-memory stages per warp
+    int ring = 0;         // shared-memory stages
     int stage_bytes = 0;  // stage stride
     int ctas = 0;         // resident CTAs per SM with that ring
 };
@@ -36,29 +36,38 @@ int group_index(int g) { return g == 32 ? 0 : g == 64 ? 1 : 2; }
 
 struct DeviceInfo {
     int sms = 0;
-    RingCfg ring[9][3][3];  // decode kernel ring by [bits][group index][mt]
     bool ok = false;
     bool is_sm103 = false;
+    std::mutex mu;
+    RingCfg ring[9][3][3][DEC_MAX_SU + 1];  // by [bits][group index][mt][su], filled on first use
 };
 
-// The decode ring: as many stages per warp as fit in about 200 KB of shared
-// memory per SM at the occupancy the kernel's registers allow.
-RingCfg make_ring(int bits, int group, int mt) {
-    RingCfg c;
-    c.stage_bytes = (int)round_up((size_t)block_bytes(bits, group), 128);
-    const int by_regs = std::max(1, decode_ctas_per_sm(bits, mt, 0));
-    const size_t budget = 200 * 1024;
-    int ns = (int)(budget / ((size_t)by_regs * DEC_WARPS * (c.stage_bytes + 8)));
-    ns = std::max(2, std::min(ns, 16));
-    while (ns > 2 && decode_smem_bytes(ns, c.stage_bytes) > (size_t)kDecodeSmemMax) --ns;
-    c.stages = ns;
-    c.ctas = std::max(1, decode_ctas_per_sm(bits, mt, decode_smem_bytes(ns, c.stage_bytes)));
-    return c;
-}
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_once[kMaxDevices];
 
-int device_info(const DeviceInfo** out) {
+// The decode ring: enough stages that about 128 KB of weights are in flight
+// per SM at the occupancy the kernel's registers allow, within ~220 KB of
+// shared memory per SM.
+RingCfg make_ring(int bits, int group, int mt, int su) {
+    RingCfg c;
+    c.stage_bytes = (int)round_up((size_t)su * block_bytes(bits, group), 128);
+    const int by_regs = std::max(1, decode_ctas_per_sm(bits, mt, su, 0));
+    int ring = (int)((128 * 1024) / ((size_t)by_regs * c.stage_bytes));
+    ring = std::max(2, std::min(ring, 12));
+    while (ring > 2 && decode_smem_bytes(ring, c.stage_bytes, su) * by_regs > 220 * 1024) --ring;
+    while (ring > 2 && decode_smem_bytes(ring, c.stage_bytes, su) > (size_t)kDecodeSmemMax) --ring;
+    c.ring = ring;
+    c.ctas = std::max(1, decode_ctas_per_sm(bits, mt, su, decode_smem_bytes(ring, c.stage_bytes, su)));
+    return c;
+}
+
+// Blocks per stage for a depth of KB blocks: as even as possible, at most 8.
+int stage_blocks(int KB) {
+    const int per_tile = (KB + DEC_MAX_SU - 1) / DEC_MAX_SU;
+    return std::max(1, (KB + per_tile - 1) / per_tile);
+}
+
+int device_info(DeviceInfo** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return AFFQMM_E_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return AFFQMM_E_DEVICE;
@@ -71,12 +80,9 @@ int device_info(const DeviceInfo** out) {
         if (!d.is_sm103) { d.ok = true; return; }
         if (decode_allow_smem(kDecodeSmemMax) != cudaSuccess) return;
         if (prompt_allow_smem() != cudaSuccess) return;
-        for (int b : {2, 3, 4, 5, 6, 8})
-            for (int g : {32, 64, 128})
-                for (int mt = 1; mt <= 2; ++mt) d.ring[b][group_index(g)][mt] = make_ring(b, g, mt);
         d.ok = true;
     });
-    const DeviceInfo& d = g_dev[dev];
+    DeviceInfo& d = g_dev[dev];
     if (!d.ok) return AFFQMM_E_CUDA;
     if (!d.is_sm103) return AFFQMM_E_DEVICE;
     *out = &d;
@@ -104,14 +110,19 @@ struct DecodePlan {
     int grid = 0;
     int mt = 1;
     size_t ws_bytes = 0;
-    size_t smem = 0;
 };
 
+const RingCfg& ring_for(DeviceInfo& d, int bits, int group, int mt, int su) {
+    std::lock_guard<std::mutex> lock(d.mu);
+    RingCfg& c = d.ring[bits][group_index(group)][mt][su];
+    if (c.ring == 0) c = make_ring(bits, group, mt, su);
+    return c;
+}
+
 // Decomposition of a decode launch over `count` projections (M <= 16): each
-// projection's blocks are cut into as many contiguous runs as the device
-// holds resident warps of the kernel (fewer if it has fewer blocks).  The cut
-// of one projection does not depend on the others in the launch.
-int plan_decode(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan) {
+// projection's stages are cut into one run per resident CTA (fewer if it has
+// fewer stages).  The cut of one projection does not depend on the others.
+int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan) {
     std::memset(&plan->p, 0, sizeof(plan->p));
     const int bits = ws[0].bits, group = ws[0].group;
     const int64_t K = ws[0].K;
@@ -124,32 +135,32 @@ int plan_decode(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t
     p.M = (int32_t)M;
     p.block_bytes = block_bytes(bits, group);
     p.group = group;
-    const RingCfg& ring = d.ring[bits][group_index(group)][plan->mt];
-    p.stages = ring.stages;
+    p.su = stage_blocks(KB);
+    p.spt = (KB + p.su - 1) / p.su;
+    const RingCfg& ring = ring_for(d, bits, group, plan->mt, p.su);
+    p.ring = ring.ring;
     p.stage_bytes = ring.stage_bytes;
-    plan->smem = decode_smem_bytes(ring.stages, ring.stage_bytes);
-    const int64_t resident = (int64_t)d.sms * ring.ctas * DEC_WARPS;
-    int64_t warps = 0, tiles_total = 0;
+    const int64_t resident = (int64_t)d.sms * ring.ctas;
+    int64_t ctas = 0, tiles_total = 0;
     for (int i = 0; i < count; ++i) {
         DecProj& P = p.proj[i];
         P.N = ws[i].N;
         P.packed = static_cast<const uint8_t*>(ws[i].packed);
         const int64_t tiles = (ws[i].N + TILE_N - 1) / TILE_N;
-        const int64_t units = tiles * KB;
+        const int64_t stages = tiles * p.spt;
         P.tiles = (int32_t)tiles;
-        P.units = (int32_t)units;
-        P.nwarps = (int32_t)std::min<int64_t>(resident, units);
-        P.warp_begin = (int32_t)warps;
+        P.stages = (int32_t)stages;
+        P.nctas = (int32_t)std::min<int64_t>(resident, stages);
+        P.cta_begin = (int32_t)ctas;
         P.ctr_begin = (int32_t)tiles_total;
-        P.slot_begin = (int32_t)(2 * warps);
-        warps += P.nwarps;
+        P.slot_begin = (int32_t)(2 * ctas);
+        ctas += P.nctas;
         tiles_total += tiles;
     }
-    if (warps > ((int64_t)1 << 30)) return AFFQMM_E_SHAPE;
+    if (ctas > ((int64_t)1 << 30)) return AFFQMM_E_SHAPE;
     if (tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
-    p.total_warps = (int32_t)warps;
-    plan->grid = (int)((warps + DEC_WARPS - 1) / DEC_WARPS);
-    plan->ws_bytes = warps > 0 ? kSlotsOffset + (size_t)(2 * warps) * kSlotFloats * sizeof(float) : 0;
+    plan->grid = (int)ctas;
+    plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kSlotFloats * sizeof(float) : 0;
     return AFFQMM_OK;
 }
 
@@ -208,7 +219,7 @@ struct PromptPlan {
 
 // Decomposition of a prompt launch: each projection's (256-row tile, block)
 // units are cut into one run per SM (fewer if it has fewer units).
-int plan_prompt(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, PromptPlan* plan) {
+int plan_prompt(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, PromptPlan* plan) {
     std::memset(&plan->p, 0, sizeof(plan->p));
     PromptParams& p = plan->p;
     const int bits = ws[0].bits, group = ws[0].group;
@@ -243,7 +254,7 @@ int plan_prompt(const DeviceInfo& d, int count, const affqmm_weight* ws, int64_t
 }
 
 int workspace_for(int count, const affqmm_weight* ws, int64_t M, size_t* bytes) {
-    const DeviceInfo* d = nullptr;
+    DeviceInfo* d = nullptr;
     int rc = device_info(&d);
     if (rc) return rc;
     *bytes = 0;
@@ -291,7 +302,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         if (!x) return AFFQMM_E_NULL;
         if (!aligned(x, 16)) return AFFQMM_E_ALIGN;
     }
-    const DeviceInfo* d = nullptr;
+    DeviceInfo* d = nullptr;
     rc = device_info(&d);
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -11,20 +11,21 @@
 
 namespace affqmm {
 
-// One projection of a decode (M <= 16) launch.  The projection's units (one
-// 16-row x 128-deep block each, numbered tile-major) are split into `nwarps`
-// contiguous runs, one per warp; the split depends only on the projection,
-// M and the device, never on what else shares the launch.
+// One projection of a decode (M <= 16) launch.  Its 128-deep blocks are
+// grouped into "stages" of up to `su` consecutive blocks of one 16-row tile
+// (ceil(KB / su) stages per tile); the stages, numbered tile-major, are cut
+// into `nctas` contiguous runs, one per CTA.  The cut depends only on the
+// projection, M and the device, never on what else shares the launch.
 struct DecProj {
     const uint8_t* packed;
     uint16_t* y;
     int64_t N;
     int32_t tiles;        // ceil(N / 16)
-    int32_t units;        // tiles * k-blocks
-    int32_t nwarps;       // warps working on this projection (<= units)
-    int32_t warp_begin;   // first global warp of this projection
+    int32_t stages;       // tiles * stages per tile
+    int32_t nctas;        // CTAs working on this projection (<= stages)
+    int32_t cta_begin;    // first CTA of this projection in the grid
     int32_t ctr_begin;    // first merge counter (one per tile)
-    int32_t slot_begin;   // first partial slot (two per warp)
+    int32_t slot_begin;   // first partial slot (two per CTA)
 };
 
 struct DecParams {
@@ -35,21 +36,23 @@ struct DecParams {
     int32_t M;
     int32_t block_bytes;     // bytes of one (tile, k-block) block
     int32_t group;
-    int32_t total_warps;
-    int32_t stages;          // shared-memory ring depth per warp
-    int32_t stage_bytes;     // ring stage stride (block_bytes rounded up to 128)
+    int32_t su;              // blocks per stage = consumer warps per CTA
+    int32_t spt;             // stages per tile = ceil(KB / su)
+    int32_t ring;            // stages in the shared-memory ring
+    int32_t stage_bytes;     // ring stage stride (su * block_bytes rounded up to 128)
     const uint16_t* x;
     uint32_t* status;        // device status word (bit 0: a bounded wait gave up)
     uint32_t* counters;
     float* partials;         // slot = 32 lanes x 8 floats
 };
 
-// Shared memory of one decode CTA for a given ring.
-inline size_t decode_smem_bytes(int stages, int stage_bytes) {
-    return (size_t)4 * stages * (stage_bytes + 8) + 16;
+// Dynamic shared memory of one decode CTA: the ring, two reduction buffers
+// (su warps x 32 lanes x 8 floats) and the mbarriers.
+inline size_t decode_smem_bytes(int ring, int stage_bytes, int su) {
+    return (size_t)ring * stage_bytes + 2 * (size_t)su * 32 * 8 * sizeof(float) + (2 * (size_t)ring + 4) * 8 + 128;
 }
 
-constexpr int DEC_WARPS = 4;
+constexpr int DEC_MAX_SU = 8;   // at most 8 consumer warps (+1 producer) per decode CTA
 
 // Workspace layout shared by every kernel: a status word, then a fixed region
 // of merge counters (zero between calls: the last user of a counter resets
@@ -94,8 +97,9 @@ constexpr size_t kPromptSlotFloats = 128 * 256;
 
 // Launchers (decode.cu, pack.cu).  They return a cudaError_t of the launch.
 cudaError_t launch_decode(int bits, int mt, const DecParams& p, int grid, cudaStream_t st);
-// Resident CTAs per SM of the decode kernel with `smem` bytes of ring.
-int decode_ctas_per_sm(int bits, int mt, size_t smem);
+// Resident CTAs per SM of the decode kernel with `su` consumer warps and
+// `smem` bytes of dynamic shared memory.
+int decode_ctas_per_sm(int bits, int mt, int su, size_t smem);
 // Let every decode instantiation use up to `bytes` of dynamic shared memory.
 cudaError_t decode_allow_smem(int bytes);
 constexpr int kDecodeSmemMax = 200 * 1024;

@@ -1,27 +1,32 @@
 // decode.cu -- the memory-bound projection for M = 1..16 activation rows.
 //
-// The weight blocks of one projection (16 rows x 128 k each, stored tile-major)
-// are cut into contiguous runs, one run per warp, with all of the device's
-// resident warps busy ("stream-K" at warp granularity).  A warp streams its
-// run's blocks from HBM into its own ring of shared-memory stages with 1-D
-// bulk copies (TMA, one mbarrier per stage, every wait bounded), keeping up
-// to `stages` blocks in flight; each lane reads its fragment words back from
-// shared memory, dequantizes every weight once as
-// bf16(fma(s, q, b)) (affqmm_format.cuh) and contracts on the tensor cores
-// with mma.sync m16n8k16 (bf16 in, fp32 accumulate): the weights are the A
-// operand (16 rows x 16 k), the activation rows the B operand (8 rows, or two
-// MMAs for 9..16 rows).  Prior art: the "reg variant" lane projection of the
-// "Gemma 4 12B on the native Metal engine" page (4-bit groups in tensor-op
-// registers, K split per shape); unlike it, the weights here are rounded to
-// bf16 before the contraction, as the same page's prompt GEMM does.
+// A CTA is one producer warp and `su` (<= 8) consumer warps.  The projection's
+// 128-deep weight blocks are grouped into stages of up to `su` consecutive
+// blocks of one 16-row tile; the stages are cut into one contiguous run per
+// resident CTA ("stream-K"), so every SM streams the same number of bytes.
+// The producer moves each stage from HBM into a ring of shared-memory slots
+// with ONE 1-D bulk copy (TMA) -- a few large copies in flight keep HBM busy
+// where many small ones do not -- and consumer warp w takes block w of the
+// stage: it reads its fragment words back from shared memory, dequantizes
+// every weight once as bf16(fma(s, q, b)) (affqmm_format.cuh) and contracts
+// on the tensor cores with mma.sync m16n8k16 (bf16 in, fp32 accumulate): the
+// weights are the A operand (16 rows x 16 k), the activation rows the B
+// operand (8 rows, or two MMAs for 9..16 rows).  Prior art: the "reg
+// variant" lane projection of the "Gemma 4 12B on the native Metal engine"
+// page (4-bit groups in tensor-op registers, K split per shape); unlike it,
+// the weights here are rounded to bf16 before the contraction, as the same
+// page's prompt GEMM does.
 //
-// Reduction order is fixed: a tile whose blocks all fall in one warp's run is
-// summed in k order and stored directly; a tile cut by run boundaries gets one
-// fp32 partial per run, and the last of those warps to arrive (an atomic
-// counter, no waiting) adds the partials in run order, converts to bf16 and
-// re-zeroes the counter.  The runs depend only on the projection, M and the
-// device, so the same inputs give the same bits on every call, alone or
-// stacked with other projections.
+// Reduction order is fixed: each consumer warp sums its blocks in k order in
+// interleaved chains (k-step s of every block into chain s mod CH);
+// at the end of a tile's segment the warps' sums are added in warp order
+// through shared memory; a tile cut by CTA run boundaries gets one fp32
+// partial per run, and the last CTA to arrive (an atomic counter, no
+// waiting) adds them in run order and re-zeroes the counter.  The cut
+// depends only on the projection, M and the device, so the same inputs give
+// the same bits on every call, alone or stacked with other projections.
+// Every wait is on an mbarrier with a bounded wait; a wait that gives up sets
+// the workspace status word and the CTA stops.
 #include <cuda_bf16.h>
 
 #include "affqmm_async.cuh"
@@ -47,18 +52,28 @@ __device__ __forceinline__ void ld_x16(const uint16_t* p, uint32_t* v) {
                      : "l"(p + 8 * i));
 }
 
+// Independent accumulator chains: k-step s of a block adds into chain
+// s % CH, so several tensor-core MMAs are in flight instead of one dependent
+// sequence (four chains for up to 8 rows, two for 9..16 rows, whose two MMAs
+// per k-step are already independent).  The chains are added in a fixed
+// order when a tile segment ends.
+template <int MT>
+constexpr int dec_chains() { return MT == 1 ? 4 : 2; }
+
 template <int BITS, int MT, int S>
 __device__ __forceinline__ void kstep(const uint32_t* cw, uint32_t sg, uint32_t bg, uint32_t sg8, uint32_t bg8,
-                                      const uint32_t* xa, const uint32_t* xb, float (&acc)[MT][4]) {
+                                      const uint32_t* xa, const uint32_t* xb,
+                                      float (&acc)[dec_chains<MT>()][MT][4]) {
+    constexpr int CH = dec_chains<MT>();
     uint32_t a[4];
     dequant_kstep<BITS, S>(cw, sg, bg, sg8, bg8, a);
-    mma_16816(acc[0], a, xa[2 * S], xa[2 * S + 1]);
-    if constexpr (MT == 2) mma_16816(acc[1], a, xb[2 * S], xb[2 * S + 1]);
+    mma_16816(acc[S % CH][0], a, xa[2 * S], xa[2 * S + 1]);
+    if constexpr (MT == 2) mma_16816(acc[S % CH][1], a, xb[2 * S], xb[2 * S + 1]);
 }
 
 template <int BITS, int MT>
 __device__ __forceinline__ void block_contract(const uint32_t* cw, uint2 sb, const uint32_t* xa, const uint32_t* xb,
-                                               float (&acc)[MT][4]) {
+                                               float (&acc)[dec_chains<MT>()][MT][4]) {
     const uint32_t sg = bcast_lo(sb.x), bg = bcast_hi(sb.x);
     const uint32_t sg8 = bcast_lo(sb.y), bg8 = bcast_hi(sb.y);
     kstep<BITS, MT, 0>(cw, sg, bg, sg8, bg8, xa, xb, acc);
@@ -77,11 +92,6 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* addr, unsigned v)
     return old;
 }
 
-// The warp whose run holds unit u: the largest w with floor(w*U/PW) <= u.
-__device__ __forceinline__ int warp_of(int u, int U, int PW) {
-    return (int)(((int64_t)(u + 1) * PW - 1) / U);
-}
-
 // y[m, n] from a lane's accumulator: lane (r, t) holds n = r (+8) and
 // m = 8*mt + 2t (+1).
 template <int MT>
@@ -97,37 +107,41 @@ __device__ __forceinline__ void store_y(const DecProj& P, int M, int tile, int r
     }
 }
 
-// Publish a partial segment [seg_start, seg_end] of tile `tile` from this
-// warp's run [u0, u1): store its fp32 sums in the warp's slot, count it on the
-// tile's counter, and if it is the last of the tile's segments to arrive, add
-// all of them in run (k) order, store y and re-zero what it used.
+// The CTA whose run holds stage g of a projection with S stages cut into PC
+// runs: the largest c with floor(c*S/PC) <= g.
+__device__ __forceinline__ int cta_of(int g, int S, int PC) {
+    return (int)(((int64_t)(g + 1) * PC - 1) / S);
+}
+
+// Publish a partial tile segment of this CTA's run: store its fp32 sums in one
+// of the CTA's two slots, count it on the tile's counter, and if it is the last
+// of the tile's segments to arrive, add all of them in run (k) order, store y
+// and reset the counter.  Executed by one warp.
 template <int MT>
-__device__ __forceinline__ void publish_partial(const DecParams& p, const DecProj& P, int w, int u0, int tile,
-                                                int seg_start, int lane, const float* v_in) {
+__device__ __forceinline__ void publish_partial(const DecParams& p, const DecProj& P, int c, int tile, bool first_seg,
+                                                int lane, const float* v_in) {
     const int r = lane >> 2, t = lane & 3;
-    const int KB = p.KB;
-    const int t0 = tile * KB, t1 = t0 + KB - 1;
-    const int U = P.units, PW = P.nwarps;
-    const int slot = P.slot_begin + 2 * w + (seg_start == u0 ? 0 : 1);
+    const int S = P.stages, PC = P.nctas;
+    const int slot = P.slot_begin + 2 * c + (first_seg ? 0 : 1);
     float* sp = p.partials + (size_t)slot * 256 + lane * 8;
 #pragma unroll
     for (int j = 0; j < MT * 4; ++j) __stcg(sp + j, v_in[j]);
-    // The warp's partial is published by lane 0's release (ordered after the
-    // other lanes' stores by __syncwarp); the acquire side of the same atomic
-    // makes every earlier partial visible to the last warp to arrive.
+    // Lane 0's release publishes the warp's stores (ordered by __syncwarp);
+    // the acquire side makes every earlier partial visible to the last CTA.
     __syncwarp();
     unsigned prev = 0;
     if (lane == 0) prev = atom_add_acq_rel(&p.counters[P.ctr_begin + tile], 1u);
     __syncwarp();
     prev = __shfl_sync(0xffffffffu, prev, 0);
-    const int wf = warp_of(t0, U, PW), wl = warp_of(t1, U, PW);
-    if (prev != (unsigned)(wl - wf)) return;
+    const int g0 = tile * p.spt, g1 = g0 + p.spt - 1;
+    const int cf = cta_of(g0, S, PC), cl = cta_of(g1, S, PC);
+    if (prev != (unsigned)(cl - cf)) return;
     float v[MT * 4];
 #pragma unroll
     for (int j = 0; j < MT * 4; ++j) v[j] = 0.f;
-    for (int c = wf; c <= wl; ++c) {
-        const int bc = (int)((int64_t)c * U / PW);
-        const int sc = P.slot_begin + 2 * c + (bc >= t0 ? 0 : 1);
+    for (int cb = cf; cb <= cl; ++cb) {
+        const int b0 = (int)((int64_t)cb * S / PC);
+        const int sc = P.slot_begin + 2 * cb + (b0 >= g0 ? 0 : 1);
         const float* cp = p.partials + (size_t)sc * 256 + lane * 8;
 #pragma unroll
         for (int j = 0; j < MT * 4; ++j) v[j] += __ldcg(cp + j);
@@ -137,158 +151,206 @@ __device__ __forceinline__ void publish_partial(const DecParams& p, const DecPro
 }
 
 template <int BITS, int MT>
-__global__ void __launch_bounds__(DEC_WARPS * 32) decode_kernel(const __grid_constant__ DecParams p) {
+__global__ void __launch_bounds__((DEC_MAX_SU + 1) * 32) decode_kernel(const __grid_constant__ DecParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int r = lane >> 2, t = lane & 3;
-    const int gw = (int)blockIdx.x * DEC_WARPS + wid;
-    if (gw >= p.total_warps) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int SU = p.su, NS = p.ring, SBY = p.stage_bytes, KB = p.KB, SPT = p.spt;
+    const int bb = p.block_bytes;
+
     int pi = 0;
     for (int i = 1; i < p.nproj; ++i)
-        if (gw >= p.proj[i].warp_begin) pi = i;
+        if ((int)blockIdx.x >= p.proj[i].cta_begin) pi = i;
     const DecProj& P = p.proj[pi];
-    const int w = gw - P.warp_begin;
-    const int U = P.units, PW = P.nwarps;
-    const int u0 = (int)((int64_t)w * U / PW);
-    const int u1 = (int)((int64_t)(w + 1) * U / PW);
-    const int n = u1 - u0;
-    const int KB = p.KB;
-    const int bb = p.block_bytes;
-    const int NS = p.stages, SBY = p.stage_bytes;
-    const uint8_t* base = P.packed;
-    const int sb_off = sb_offset(BITS, p.group, t, r);
-    const bool row0 = r < p.M;
-    const bool row1 = (MT == 2) && (r + 8 < p.M);
-    const uint16_t* x0 = p.x + (size_t)r * p.K + 32 * t;
-    const uint16_t* x1 = p.x + (size_t)(r + 8) * p.K + 32 * t;
+    const int c = (int)blockIdx.x - P.cta_begin;
+    const int S = P.stages, PC = P.nctas;
+    const int g_lo = (int)((int64_t)c * S / PC);
+    const int g_hi = (int)((int64_t)(c + 1) * S / PC);
 
-    // This warp's ring: NS stages of SBY bytes, then NS mbarriers.
-    const uint32_t ring = smem_u32(smem) + (uint32_t)(wid * NS * SBY);
-    const uint32_t bars = smem_u32(smem) + (uint32_t)(DEC_WARPS * NS * SBY + wid * NS * 8);
-    if (lane == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(bars + 8 * s, 1);
+    // shared memory: ring | reduction buffers [2][SU][MT*4][32] | barriers
+    const uint32_t s_base = smem_u32(smem);
+    float* red = reinterpret_cast<float*>(smem + (size_t)NS * SBY);
+    const uint32_t bar0 = s_base + (uint32_t)((size_t)NS * SBY + 2 * (size_t)SU * 32 * 8 * sizeof(float));
+    auto bar_full = [&](int s) { return bar0 + 8u * s; };
+    auto bar_empty = [&](int s) { return bar0 + 8u * (NS + s); };
+    auto bar_red_full = [&](int b) { return bar0 + 8u * (2 * NS + b); };
+    auto bar_red_free = [&](int b) { return bar0 + 8u * (2 * NS + 2 + b); };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), SU);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_red_full(b), SU);
+            mbar_init(bar_red_free(b), 1);
+        }
         fence_mbar_init();
     }
-    __syncwarp();
-    const uint64_t policy = policy_evict_first();  // weights are read once
-    auto issue = [&](int j) {                       // unit u0 + j into stage j % NS
-        const int s = j % NS;
-        mbar_arrive_expect_tx(bars + 8 * s, (uint32_t)bb);
-        bulk_g2s_hint(ring + (uint32_t)(s * SBY), base + (size_t)(u0 + j) * bb, (uint32_t)bb, bars + 8 * s, policy);
-    };
-    if (lane == 0)
-        for (int j = 0; j < NS && j < n; ++j) issue(j);
+    __syncthreads();
 
-    float acc[MT][4];
-#pragma unroll
-    for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    int tile = u0 / KB;
-    int kb = u0 - tile * KB;
-    int seg_start = u0;
-    int stage = 0;
-    uint32_t parity = 0;
-    int j = 0;
-    // partial segments of this run, published after it
-    float first_v[MT * 4], last_v[MT * 4];
-    int first_tile = -1, last_tile = -1, last_start = 0;
-    for (; j < n; ++j) {
-        const int u = u0 + j;
-        const bool ok = mbar_wait(bars + 8 * stage, parity);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        uint32_t cw[2 * BITS];
-        const uint32_t blk = ring + (uint32_t)(stage * SBY);
-        load_lane_codes_smem<BITS>(blk, lane, cw);
-        uint2 sb;
-        lds_v2(blk + sb_off, sb.x, sb.y);
-        uint32_t xa[16], xb[16];
-        const int64_t kpos = (int64_t)kb * KBLK;
-        const bool kin = kpos + 32 * t < p.K;
-        if (row0 && kin) {
-            ld_x16(x0 + kpos, xa);
-        } else {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) xa[q] = 0u;
-        }
-        if constexpr (MT == 2) {
-            if (row1 && kin) {
-                ld_x16(x1 + kpos, xb);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 16; ++q) xb[q] = 0u;
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();  // the weights are read once
+            int s = 0;
+            uint32_t ph = 0;
+            const int tile0 = g_lo / SPT;
+            int kb0 = (g_lo - tile0 * SPT) * SU;
+            const uint8_t* src = P.packed + ((size_t)tile0 * KB + kb0) * bb;  // stages are contiguous
+            for (int g = g_lo; g < g_hi; ++g) {
+                if (!mbar_wait(bar_empty(s), ph ^ 1u)) {
+                    atomicOr(p.status, 1u);
+                    break;
+                }
+                const int cnt = min(SU, KB - kb0);
+                const uint32_t bytes = (uint32_t)(cnt * bb);
+                mbar_arrive_expect_tx(bar_full(s), bytes);
+                bulk_g2s_hint(s_base + (uint32_t)(s * SBY), src, bytes, bar_full(s), policy);
+                src += bytes;
+                kb0 = (kb0 + cnt == KB) ? 0 : kb0 + SU;
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
-        // every lane has its words in registers: refill this stage NS units ahead
-        __syncwarp();
-        if (lane == 0 && j + NS < n) {
-            fence_proxy_async_smem();
-            issue(j + NS);
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int cw = warp - 1;  // block cw of every stage
+    const int r = lane >> 2, t = lane & 3;
+    const int sb_off = sb_offset(BITS, p.group, t, r);
+    // Activation rows past M feed only output columns that are never stored,
+    // so those lanes read row 0 instead of branching around the load.
+    const uint16_t* x0 = p.x + (size_t)(r < p.M ? r : 0) * p.K + 32 * t;
+    const uint16_t* x1 = p.x + (size_t)(r + 8 < p.M ? r + 8 : 0) * p.K + 32 * t;
+    const bool ragged_k = (p.K % KBLK) != 0;  // only then can a lane's 32 k pass K
+
+    constexpr int CH = dec_chains<MT>();
+    float acc[CH][MT][4];
+#pragma unroll
+    for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+        for (int i = 0; i < MT; ++i) acc[ch][i][0] = acc[ch][i][1] = acc[ch][i][2] = acc[ch][i][3] = 0.f;
+    float first_v[MT * 4];
+    int first_tile = -1;
+    int seg = 0;                 // tile segments finished by this CTA
+    int seg_first_g = g_lo;      // first stage of the current segment
+    bool failed = false;
+    int s = 0;
+    uint32_t ph = 0;
+    int tile = g_lo / SPT;
+    int kb0 = (g_lo - tile * SPT) * SU;
+    for (int g = g_lo; g < g_hi; ++g) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(s), ph))) {
+            failed = true;
+            break;
         }
-        block_contract<BITS, MT>(cw, sb, xa, xb, acc);
-        if (kb == KB - 1 || u == u1 - 1) {
+        const int cnt = min(SU, KB - kb0);
+        if (cw < cnt) {
+            const uint32_t blk = s_base + (uint32_t)(s * SBY + cw * bb);
+            uint32_t cw_words[2 * BITS];
+            load_lane_codes_smem<BITS>(blk, lane, cw_words);
+            uint2 sb;
+            lds_v2(blk + sb_off, sb.x, sb.y);
+            uint32_t xa[16], xb[16];
+            const int kpos = (kb0 + cw) * KBLK;
+            if (!ragged_k || kpos + 32 * t < p.K) {
+                ld_x16(x0 + kpos, xa);
+                if constexpr (MT == 2) ld_x16(x1 + kpos, xb);
+            } else {  // depth padding: the weights there are zero, so are these
+#pragma unroll
+                for (int q = 0; q < 16; ++q) xa[q] = xb[q] = 0u;
+            }
+            block_contract<BITS, MT>(cw_words, sb, xa, xb, acc);
+        }
+        // this warp is done with the stage's shared memory
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty(s));
+
+        const bool tile_end = kb0 + cnt == KB;
+        const int cur_tile = tile;
+        kb0 = tile_end ? 0 : kb0 + SU;
+        tile += tile_end ? 1 : 0;
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+        if (!(tile_end || g == g_hi - 1)) continue;
+        // ---- end of a tile segment: add the warps' sums in warp order
+        const int b = seg & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_red_free(b), (uint32_t)((seg >> 1) & 1) ^ 1u))) {
+            failed = true;
+            break;
+        }
+        float* rb = red + (size_t)b * SU * 32 * 8;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                rb[((size_t)cw * 8 + mt * 4 + q) * 32 + lane] =
+                    CH == 4 ? (acc[0][mt][q] + acc[1][mt][q]) + (acc[CH > 2 ? 2 : 0][mt][q] + acc[CH - 1][mt][q])
+                            : acc[0][mt][q] + acc[1][mt][q];
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) acc[ch][mt][0] = acc[ch][mt][1] = acc[ch][mt][2] = acc[ch][mt][3] = 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_red_full(b));
+        if (cw == 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_red_full(b), (uint32_t)((seg >> 1) & 1)))) {
+                failed = true;
+                break;
+            }
             float v[MT * 4];
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int j = 0; j < MT * 4; ++j) {
+                float sum = rb[(size_t)j * 32 + lane];
+                for (int w = 1; w < SU; ++w) sum += rb[((size_t)w * 8 + j) * 32 + lane];
+                v[j] = sum;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_red_free(b));
+            const bool whole = (seg_first_g == cur_tile * SPT) && tile_end;
+            if (whole) {
+                store_y<MT>(P, p.M, cur_tile, r, t, v);
+            } else if (seg_first_g == g_lo && g != g_hi - 1) {
+                // the run's first segment ends mid-run: publish it after the
+                // run so the stream never waits on a merge
 #pragma unroll
-                for (int i = 0; i < 4; ++i) v[mt * 4 + i] = acc[mt][i];
-            if (seg_start == tile * KB && kb == KB - 1) {
-                store_y<MT>(P, p.M, tile, r, t, v);  // the whole tile was ours
-            } else if (seg_start == u0 && u != u1 - 1) {
-                // the run's first segment ends mid-run: keep it in registers and
-                // publish it after the run, so the stream never stalls on a merge
-#pragma unroll
-                for (int q = 0; q < MT * 4; ++q) first_v[q] = v[q];
-                first_tile = tile;
+                for (int j = 0; j < MT * 4; ++j) first_v[j] = v[j];
+                first_tile = cur_tile;
             } else {
-                last_tile = tile;
-                last_start = seg_start;
-#pragma unroll
-                for (int q = 0; q < MT * 4; ++q) last_v[q] = v[q];
-            }
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-            seg_start = u + 1;
-        }
-        if (++kb == KB) {
-            kb = 0;
-            ++tile;
-        }
-        if (++stage == NS) {
-            stage = 0;
-            parity ^= 1u;
-        }
-    }
-    if (j == n) {
-        if (first_tile >= 0) publish_partial<MT>(p, P, w, u0, first_tile, u0, lane, first_v);
-        if (last_tile >= 0) publish_partial<MT>(p, P, w, u0, last_tile, last_start, lane, last_v);
-    } else {
-        // A bounded wait gave up: record it and let the copies still in flight
-        // land (again bounded) before this CTA's shared memory is released.
-        if (lane == 0) {
-            atomicOr(p.status, 1u);
-            for (int q = j; q < n && q < j + NS; ++q) {
-                const int s = q % NS;
-                (void)mbar_wait(bars + 8 * s, (uint32_t)((q / NS) & 1));
+                publish_partial<MT>(p, P, c, cur_tile, seg_first_g == g_lo, lane, v);
             }
         }
-        __syncwarp();
+        ++seg;
+        seg_first_g = g + 1;
     }
+    if (failed) {
+        if (lane == 0) atomicOr(p.status, 1u);
+        return;
+    }
+    if (cw == 0 && first_tile >= 0) publish_partial<MT>(p, P, c, first_tile, true, lane, first_v);
 }
 
 template <int BITS>
 cudaError_t launch_bits(int mt, const DecParams& p, int grid, cudaStream_t st) {
-    const size_t smem = decode_smem_bytes(p.stages, p.stage_bytes);
+    const size_t smem = decode_smem_bytes(p.ring, p.stage_bytes, p.su);
+    const int threads = (p.su + 1) * 32;
     if (mt == 1)
-        decode_kernel<BITS, 1><<<grid, DEC_WARPS * 32, smem, st>>>(p);
+        decode_kernel<BITS, 1><<<grid, threads, smem, st>>>(p);
     else
-        decode_kernel<BITS, 2><<<grid, DEC_WARPS * 32, smem, st>>>(p);
+        decode_kernel<BITS, 2><<<grid, threads, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 template <int BITS>
-int occupancy_bits(int mt, size_t smem) {
+int occupancy_bits(int mt, int su, size_t smem) {
     int n = 0;
-    cudaError_t e = mt == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS, 1>, DEC_WARPS * 32, smem)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS, 2>, DEC_WARPS * 32, smem);
+    const int threads = (su + 1) * 32;
+    cudaError_t e = mt == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS, 1>, threads, smem)
+                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS, 2>, threads, smem);
     return e == cudaSuccess ? n : -1;
 }
 
@@ -313,14 +375,14 @@ cudaError_t launch_decode(int bits, int mt, const DecParams& p, int grid, cudaSt
     }
 }
 
-int decode_ctas_per_sm(int bits, int mt, size_t smem) {
+int decode_ctas_per_sm(int bits, int mt, int su, size_t smem) {
     switch (bits) {
-        case 2: return occupancy_bits<2>(mt, smem);
-        case 3: return occupancy_bits<3>(mt, smem);
-        case 4: return occupancy_bits<4>(mt, smem);
-        case 5: return occupancy_bits<5>(mt, smem);
-        case 6: return occupancy_bits<6>(mt, smem);
-        case 8: return occupancy_bits<8>(mt, smem);
+        case 2: return occupancy_bits<2>(mt, su, smem);
+        case 3: return occupancy_bits<3>(mt, su, smem);
+        case 4: return occupancy_bits<4>(mt, su, smem);
+        case 5: return occupancy_bits<5>(mt, su, smem);
+        case 6: return occupancy_bits<6>(mt, su, smem);
+        case 8: return occupancy_bits<8>(mt, su, smem);
         default: return -1;
     }
 }
