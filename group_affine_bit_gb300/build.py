@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libaffqmm.so")
 
 SOURCES = ["affqmm_api.cu", "pack.cu", "decode.cu", "prompt.cu"]
-HEADERS = ["affqmm_format.cuh", "affqmm_internal.h", "affqmm_async.cuh"]
+HEADERS = ["affqmm_format.cuh", "affqmm_internal.h", "affqmm_async.cuh", "affqmm_tc.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

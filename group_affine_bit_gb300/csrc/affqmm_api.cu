@@ -17,55 +17,26 @@ using namespace affqmm;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kSlotFloats = 256;    // one decode partial: 32 lanes x 8 floats
 
 bool valid_bits(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
 bool valid_group(int g) { return g == 32 || g == 64 || g == 128; }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Per-device facts the decomposition depends on (a cache of queries, not state
 // that changes what a call computes on a given device).
-struct RingCfg {
-    int ring = 0;         // shared-memory stages
-    int stage_bytes = 0;  // stage stride
-    int ctas = 0;         // resident CTAs per SM with that ring
-};
-
-int group_index(int g) { return g == 32 ? 0 : g == 64 ? 1 : 2; }
-
 struct DeviceInfo {
     int sms = 0;
     bool ok = false;
     bool is_sm103 = false;
-    std::mutex mu;
-    RingCfg ring[9][3][3][DEC_MAX_SU + 1];  // by [bits][group index][mt][su], filled on first use
 };
-
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_once[kMaxDevices];
 
-// The decode ring: enough stages that about 128 KB of weights are in flight
-// per SM at the occupancy the kernel's registers allow, within ~220 KB of
-// shared memory per SM.
-RingCfg make_ring(int bits, int group, int mt, int su) {
-    RingCfg c;
-    c.stage_bytes = (int)round_up((size_t)su * block_bytes(bits, group), 128);
-    const int by_regs = std::max(1, decode_ctas_per_sm(bits, mt, su, 0));
-    int ring = (int)((128 * 1024) / ((size_t)by_regs * c.stage_bytes));
-    ring = std::max(2, std::min(ring, 12));
-    while (ring > 2 && decode_smem_bytes(ring, c.stage_bytes, su) * by_regs > 220 * 1024) --ring;
-    while (ring > 2 && decode_smem_bytes(ring, c.stage_bytes, su) > (size_t)kDecodeSmemMax) --ring;
-    c.ring = ring;
-    c.ctas = std::max(1, decode_ctas_per_sm(bits, mt, su, decode_smem_bytes(ring, c.stage_bytes, su)));
-    return c;
-}
-
-// Blocks per stage for a depth of KB blocks: as even as possible, at most 8.
-int stage_blocks(int KB) {
-    const int per_tile = (KB + DEC_MAX_SU - 1) / DEC_MAX_SU;
-    return std::max(1, (KB + per_tile - 1) / per_tile);
-}
+// Decode kernel shape: a ring of 4 stages (weight block + activation tile
+// each) and two CTAs per SM -- each CTA holds 256 of the SM's 512
+// tensor-memory columns.  That keeps 70-150 KB of weights in flight per SM.
+constexpr int kDecRing = 4;
+constexpr int kDecCtasPerSm = 2;
 
 int device_info(DeviceInfo** out) {
     int dev = 0;
@@ -78,7 +49,7 @@ int device_info(DeviceInfo** out) {
         d.sms = prop.multiProcessorCount;
         d.is_sm103 = prop.major == 10 && prop.minor == 3;
         if (!d.is_sm103) { d.ok = true; return; }
-        if (decode_allow_smem(kDecodeSmemMax) != cudaSuccess) return;
+        if (decode_allow_smem() != cudaSuccess) return;
         if (prompt_allow_smem() != cudaSuccess) return;
         d.ok = true;
     });
@@ -108,59 +79,42 @@ int check_weight(const affqmm_weight* w) {
 struct DecodePlan {
     DecParams p;
     int grid = 0;
-    int mt = 1;
     size_t ws_bytes = 0;
 };
 
-const RingCfg& ring_for(DeviceInfo& d, int bits, int group, int mt, int su) {
-    std::lock_guard<std::mutex> lock(d.mu);
-    RingCfg& c = d.ring[bits][group_index(group)][mt][su];
-    if (c.ring == 0) c = make_ring(bits, group, mt, su);
-    return c;
-}
-
 // Decomposition of a decode launch over `count` projections (M <= 16): each
-// projection's stages are cut into one run per resident CTA (fewer if it has
-// fewer stages).  The cut of one projection does not depend on the others.
+// projection's (128-row tile, 128-deep block) units are cut into one run per
+// resident CTA (fewer if it has fewer units).  The cut of one projection does
+// not depend on the others in the launch.
 int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan) {
     std::memset(&plan->p, 0, sizeof(plan->p));
-    const int bits = ws[0].bits, group = ws[0].group;
     const int64_t K = ws[0].K;
     const int KB = (int)((K + KBLK - 1) / KBLK);
-    plan->mt = M > 8 ? 2 : 1;
     DecParams& p = plan->p;
     p.nproj = count;
     p.KB = KB;
     p.K = K;
     p.M = (int32_t)M;
-    p.block_bytes = block_bytes(bits, group);
-    p.group = group;
-    p.su = stage_blocks(KB);
-    p.spt = (KB + p.su - 1) / p.su;
-    const RingCfg& ring = ring_for(d, bits, group, plan->mt, p.su);
-    p.ring = ring.ring;
-    p.stage_bytes = ring.stage_bytes;
-    const int64_t resident = (int64_t)d.sms * ring.ctas;
+    p.ring = kDecRing;
+    const int64_t resident = (int64_t)d.sms * kDecCtasPerSm;
     int64_t ctas = 0, tiles_total = 0;
     for (int i = 0; i < count; ++i) {
         DecProj& P = p.proj[i];
         P.N = ws[i].N;
         P.packed = static_cast<const uint8_t*>(ws[i].packed);
         const int64_t tiles = (ws[i].N + TILE_N - 1) / TILE_N;
-        const int64_t stages = tiles * p.spt;
         P.tiles = (int32_t)tiles;
-        P.stages = (int32_t)stages;
-        P.nctas = (int32_t)std::min<int64_t>(resident, stages);
+        P.units = (int32_t)(tiles * KB);
+        P.nctas = (int32_t)std::min<int64_t>(resident, P.units);
         P.cta_begin = (int32_t)ctas;
         P.ctr_begin = (int32_t)tiles_total;
         P.slot_begin = (int32_t)(2 * ctas);
         ctas += P.nctas;
         tiles_total += tiles;
     }
-    if (ctas > ((int64_t)1 << 30)) return AFFQMM_E_SHAPE;
-    if (tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
+    if (4 * tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
     plan->grid = (int)ctas;
-    plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kSlotFloats * sizeof(float) : 0;
+    plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kDecSlotFloats * sizeof(float) : 0;
     return AFFQMM_OK;
 }
 
@@ -196,14 +150,14 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// x [M, K] bf16 row-major as 64 (k) x 128 (rows) boxes with the 128-byte
+// x [M, K] bf16 row-major as 64 (k) x `box_rows` boxes with the 128-byte
 // swizzle the tensor core reads; rows past M and k past K read as zero.
-int make_x_map(const uint16_t* x, int64_t M, int64_t K, CUtensorMap* map) {
+int make_x_map(const uint16_t* x, int64_t M, int64_t K, int box_rows, CUtensorMap* map) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return AFFQMM_E_CUDA;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -236,7 +190,7 @@ int plan_prompt(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, Pr
         PromptProj& P = p.proj[i];
         P.N = ws[i].N;
         P.packed = static_cast<const uint8_t*>(ws[i].packed);
-        P.tiles16 = (int32_t)((ws[i].N + TILE_N - 1) / TILE_N);
+        P.ltiles = (int32_t)((ws[i].N + TILE_N - 1) / TILE_N);
         const int64_t tiles = (ws[i].N + kPromptTileN - 1) / kPromptTileN;
         P.tiles = (int32_t)tiles;
         P.units = (int32_t)(tiles * KB);
@@ -324,9 +278,11 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         rc = plan_decode(*d, count, ws, M, &plan);
         if (rc) return rc;
         bind_workspace(&plan, workspace);
-        plan.p.x = x;
         for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i];
-        if (launch_decode(ws[0].bits, plan.mt, plan.p, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
+        CUtensorMap map;
+        rc = make_x_map(x, M, K, 16, &map);
+        if (rc) return rc;
+        if (launch_decode(ws[0].bits, ws[0].group, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
         return AFFQMM_OK;
     }
     // Prompt rows: chunks of up to 128 rows on the tensor-core kernel.
@@ -341,7 +297,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         plan.p.slots = reinterpret_cast<float*>(wsb + kSlotsOffset);
         for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i] ? ys[i] + m0 * ws[i].N : nullptr;
         CUtensorMap map;
-        rc = make_x_map(x + m0 * K, mc, K, &map);
+        rc = make_x_map(x + m0 * K, mc, K, 128, &map);
         if (rc) return rc;
         if (launch_prompt(ws[0].bits, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
     }

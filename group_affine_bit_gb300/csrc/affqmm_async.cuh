@@ -88,14 +88,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return true;
 }
 
-// 16 / 8 byte shared-memory loads at a 32-bit shared address.
-__device__ __forceinline__ void lds_v4(uint32_t a, uint32_t& x, uint32_t& y, uint32_t& z, uint32_t& w) {
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(x), "=r"(y), "=r"(z), "=r"(w) : "r"(a) : "memory");
-}
-__device__ __forceinline__ void lds_v2(uint32_t a, uint32_t& x, uint32_t& y) {
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(x), "=r"(y) : "r"(a) : "memory");
-}
-
 #endif  // __CUDACC__
 
 }  // namespace affqmm

@@ -11,48 +11,38 @@
 
 namespace affqmm {
 
-// One projection of a decode (M <= 16) launch.  Its 128-deep blocks are
-// grouped into "stages" of up to `su` consecutive blocks of one 16-row tile
-// (ceil(KB / su) stages per tile); the stages, numbered tile-major, are cut
-// into `nctas` contiguous runs, one per CTA.  The cut depends only on the
-// projection, M and the device, never on what else shares the launch.
+// One projection of a decode (M <= 16) launch: its units are
+// (128-row tile, 128-deep block) pairs, numbered tile-major (the order they
+// sit in memory), cut into `nctas` contiguous runs, one per CTA.  The cut
+// depends only on the projection, M and the device, never on what else
+// shares the launch.
 struct DecProj {
     const uint8_t* packed;
     uint16_t* y;
     int64_t N;
-    int32_t tiles;        // ceil(N / 16)
-    int32_t stages;       // tiles * stages per tile
-    int32_t nctas;        // CTAs working on this projection (<= stages)
+    int32_t tiles;        // ceil(N / 128)
+    int32_t units;        // tiles * k-blocks
+    int32_t nctas;        // CTAs working on this projection (<= units)
     int32_t cta_begin;    // first CTA of this projection in the grid
-    int32_t ctr_begin;    // first merge counter (one per tile)
+    int32_t ctr_begin;    // first tile of this projection's merge counters (four per tile)
     int32_t slot_begin;   // first partial slot (two per CTA)
 };
+
+constexpr int kDecMaxRing = 8;
 
 struct DecParams {
     DecProj proj[AFFQMM_MAX_STACK];
     int32_t nproj;
     int32_t KB;              // k-blocks of 128
     int64_t K;
-    int32_t M;
-    int32_t block_bytes;     // bytes of one (tile, k-block) block
-    int32_t group;
-    int32_t su;              // blocks per stage = consumer warps per CTA
-    int32_t spt;             // stages per tile = ceil(KB / su)
-    int32_t ring;            // stages in the shared-memory ring
-    int32_t stage_bytes;     // ring stage stride (su * block_bytes rounded up to 128)
-    const uint16_t* x;
+    int32_t M;               // activation rows (1..16)
+    int32_t ring;            // shared-memory stages (<= kDecMaxRing)
     uint32_t* status;        // device status word (bit 0: a bounded wait gave up)
     uint32_t* counters;
-    float* partials;         // slot = 32 lanes x 8 floats
+    float* partials;         // slot = 128 rows x 16 floats
 };
 
-// Dynamic shared memory of one decode CTA: the ring, two reduction buffers
-// (su warps x 32 lanes x 8 floats) and the mbarriers.
-inline size_t decode_smem_bytes(int ring, int stage_bytes, int su) {
-    return (size_t)ring * stage_bytes + 2 * (size_t)su * 32 * 8 * sizeof(float) + (2 * (size_t)ring + 4) * 8 + 128;
-}
-
-constexpr int DEC_MAX_SU = 8;   // at most 8 consumer warps (+1 producer) per decode CTA
+constexpr size_t kDecSlotFloats = 128 * 16;
 
 // Workspace layout shared by every kernel: a status word, then a fixed region
 // of merge counters (zero between calls: the last user of a counter resets
@@ -71,7 +61,7 @@ struct PromptProj {
     const uint8_t* packed;
     uint16_t* y;
     int64_t N;
-    int32_t tiles16;      // ceil(N / 16): 16-row blocks present in `packed`
+    int32_t ltiles;       // ceil(N / 128): 128-row layout tiles present in `packed`
     int32_t tiles;        // ceil(N / 256)
     int32_t units;        // tiles * k-blocks
     int32_t nctas;        // CTAs working on this projection (<= units)
@@ -95,13 +85,11 @@ struct PromptParams {
 
 constexpr size_t kPromptSlotFloats = 128 * 256;
 
-// Launchers (decode.cu, pack.cu).  They return a cudaError_t of the launch.
-cudaError_t launch_decode(int bits, int mt, const DecParams& p, int grid, cudaStream_t st);
-// Resident CTAs per SM of the decode kernel with `su` consumer warps and
-// `smem` bytes of dynamic shared memory.
-int decode_ctas_per_sm(int bits, int mt, int su, size_t smem);
-// Let every decode instantiation use up to `bytes` of dynamic shared memory.
-cudaError_t decode_allow_smem(int bytes);
+// Launchers (decode.cu, prompt.cu, pack.cu).  They return the launch's error.
+// decode.cu: the tensor map describes x [M, K] bf16 with a 64 x 16 box.
+size_t decode_smem_bytes(int bits, int group, int ring);
+cudaError_t decode_allow_smem();
+cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st);
 constexpr int kDecodeSmemMax = 200 * 1024;
 // prompt.cu: the tensor map describes x [M, K] bf16 with a 64 x 128 box.
 size_t prompt_smem_bytes();

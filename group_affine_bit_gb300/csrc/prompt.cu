@@ -6,8 +6,9 @@
 // Per unit:
 //   * a TMA warp loads the 128 x 128 activation tile (two 64-wide panels,
 //     128-byte swizzle, rows past M and depth past K filled with zeros);
-//   * eight dequantization warps read the unit's sixteen packed 16-row blocks
-//     from HBM (one unit ahead, in registers), round every weight once as
+//   * eight dequantization warps, one thread per weight row, read the row's
+//     codes of the unit's two packed 128-row blocks from HBM (one unit
+//     ahead, in registers), round every weight once as
 //     bf16(fma(s, q, b)) -- the same device arithmetic as the decode kernel
 //     -- and write them into shared memory in the tensor core's K-major,
 //     128-byte-swizzled layout (prior art: the affine_mm prompt GEMM of the
@@ -33,6 +34,7 @@
 #include "affqmm_async.cuh"
 #include "affqmm_format.cuh"
 #include "affqmm_internal.h"
+#include "affqmm_tc.cuh"
 
 namespace affqmm {
 namespace {
@@ -50,82 +52,23 @@ constexpr uint32_t P_A_PANEL = P_TILE_M * 128;         // one 64-deep panel
 constexpr uint32_t P_B_PANEL = P_TILE_N * 128;
 constexpr uint32_t P_TMEM_COLS = 256;
 
-// instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major,
-// N = 256, M = 128
-constexpr uint32_t P_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(P_TILE_N >> 3) << 17) |
-                             ((uint32_t)(P_TILE_M >> 4) << 24);
-
-// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
-// whose 8-row groups are 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
-    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
-           ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+constexpr uint32_t P_IDESC = idesc_bf16_f32(P_TILE_M, P_TILE_N);
 
 __device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel_p(unsigned* addr, unsigned v) {
-    unsigned old;
-    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
-    return old;
-}
-
-// A bounded wait that also gives up when another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
-            *abort_flag = 1;
-            atomicOr(status, 1u);
-            return false;
-        }
+// The 16 chunks (8 weights each) of one dequantized row into the 128-byte-
+// swizzled K-major layout: chunk c holds k = 8c .. 8c + 7, lives in panel
+// c / 8 at 16-byte position (c mod 8) xor (row mod 8) of the row's 128 bytes.
+template <int BITS, int GROUP, int C>
+__device__ __forceinline__ void store_chunks(const uint32_t* cw, const uint32_t* sbw, uint32_t rowbase, int r8) {
+    if constexpr (C < KBLK / 8) {
+        uint32_t w[4];
+        weight_pairs<BITS, GROUP, 4 * C, 4>(cw, sbw, w);
+        sts_v4(rowbase + (uint32_t)(C >> 3) * P_B_PANEL + ((uint32_t)((C & 7) ^ r8) << 4), w[0], w[1], w[2], w[3]);
+        store_chunks<BITS, GROUP, C + 1>(cw, sbw, rowbase, r8);
     }
-    return true;
 }
 
 struct PromptSmem {
@@ -138,7 +81,7 @@ struct PromptSmem {
     int abort_flag;
 };
 
-template <int BITS>
+template <int BITS, int GROUP>
 __global__ void __launch_bounds__(P_THREADS, 1)
     prompt_kernel(const __grid_constant__ PromptParams p, const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ uint8_t smem_raw[];
@@ -178,13 +121,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         sh->abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {  // TMEM for the fp32 accumulator: 128 lanes x 256 columns
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         sh_addr + (uint32_t)offsetof(PromptSmem, tmem_base)),
-                     "r"(P_TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1)  // TMEM for the fp32 accumulator: 128 lanes x 256 columns
+        tmem_alloc(sh_addr + (uint32_t)offsetof(PromptSmem, tmem_base), P_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -194,7 +132,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+            prefetch_tmap(&xmap);
             for (int u = u0, i = 0; u < u1; ++u, ++i) {
                 const int s = i % P_STAGES;
                 const uint32_t ph = (uint32_t)((i / P_STAGES) & 1);
@@ -229,7 +167,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = sw128_desc(stage_a(s) + pnl * P_A_PANEL + kk * 32);
                         const uint64_t bd = sw128_desc(stage_b(s) + pnl * P_B_PANEL + kk * 32);
-                        umma_f16(tmem, ad, bd, P_IDESC, (first && pnl == 0 && kk == 0) ? 0u : 1u);
+                        umma_ss(tmem, ad, bd, P_IDESC, (first && pnl == 0 && kk == 0) ? 0u : 1u);
                     }
                 }
                 umma_commit(bar_empty(s));
@@ -242,59 +180,31 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         }
     } else if (warp < P_EPI_WARP0) {
         // ---------------------------------------------------------- dequantization
-        const int dw = warp - P_DEQ_WARP0;            // sub-tiles 2*dw, 2*dw + 1 of 16
-        const int q = lane >> 3, j = lane & 7;        // conflict-free store order
-        const int pl = 4 * j + q;                     // the packed lane this thread reads
-        const int r = j, t = q;
-        const int sb_off = sb_offset(BITS, p.group, t, r);
-        const int bb = p.block_bytes;
-        uint32_t cw[2][2][2 * BITS];
-        uint2 sb[2][2];
+        // thread = weight row n of the 256-row tile (two 128-row layout tiles)
+        const int n = 32 * (warp - P_DEQ_WARP0) + lane;
+        const int sub = n >> 7, nn = n & 127;
+        constexpr int BB = block_bytes(BITS, GROUP);
+        uint32_t cw[2][4 * BITS];
+        uint32_t sbw[2][sb_words(GROUP)];
         auto load_unit = [&](int u, auto bufc) {
             constexpr int buf = decltype(bufc)::value;
             const int tile = u / KB, kb = u % KB;
+            const int lt = 2 * tile + sub;  // layout tile of this row
+            if (lt < P.ltiles) {
+                const uint8_t* blk = P.packed + ((size_t)lt * KB + kb) * BB;
+                load_row_codes<BITS>(blk, nn, cw[buf]);
+                load_row_sb<GROUP>(blk + sb_offset(BITS, GROUP, nn), sbw[buf]);
+            } else {  // rows past the last tile: zero weights
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int st = tile * (P_TILE_N / TILE_N) + 2 * dw + h;
-                if (st < P.tiles16) {
-                    const uint8_t* blk = P.packed + ((size_t)st * KB + kb) * bb;
-                    load_lane_codes<BITS>(blk, pl, cw[buf][h]);
-                    uint32_t a, b2;
-                    ld_stream_v2(blk + sb_off, a, b2);
-                    sb[buf][h] = make_uint2(a, b2);
-                } else {
+                for (int w = 0; w < 4 * BITS; ++w) cw[buf][w] = 0u;
 #pragma unroll
-                    for (int w = 0; w < 2 * BITS; ++w) cw[buf][h][w] = 0u;
-                    sb[buf][h] = make_uint2(0u, 0u);
-                }
+                for (int w = 0; w < sb_words(GROUP); ++w) sbw[buf][w] = 0u;
             }
         };
         auto store_unit = [&](int s, auto bufc) {
             constexpr int buf = decltype(bufc)::value;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t sg = bcast_lo(sb[buf][h].x), bg = bcast_hi(sb[buf][h].x);
-                const uint32_t sg8 = bcast_lo(sb[buf][h].y), bg8 = bcast_hi(sb[buf][h].y);
-                uint32_t a[8][4];
-                dequant_kstep<BITS, 0>(cw[buf][h], sg, bg, sg8, bg8, a[0]);
-                dequant_kstep<BITS, 1>(cw[buf][h], sg, bg, sg8, bg8, a[1]);
-                dequant_kstep<BITS, 2>(cw[buf][h], sg, bg, sg8, bg8, a[2]);
-                dequant_kstep<BITS, 3>(cw[buf][h], sg, bg, sg8, bg8, a[3]);
-                dequant_kstep<BITS, 4>(cw[buf][h], sg, bg, sg8, bg8, a[4]);
-                dequant_kstep<BITS, 5>(cw[buf][h], sg, bg, sg8, bg8, a[5]);
-                dequant_kstep<BITS, 6>(cw[buf][h], sg, bg, sg8, bg8, a[6]);
-                dequant_kstep<BITS, 7>(cw[buf][h], sg, bg, sg8, bg8, a[7]);
-                const int n0 = 16 * (2 * dw + h) + r;  // row r of the sub-tile; row r + 8 is n0 + 8
-                const uint32_t pbase = stage_b(s) + (uint32_t)(t >> 1) * P_B_PANEL;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t chunk = (uint32_t)((4 * (t & 1) + i) ^ r) << 4;
-                    sts_v4(pbase + (uint32_t)(n0 >> 3) * 1024u + (uint32_t)r * 128u + chunk, a[2 * i][0],
-                           a[2 * i][2], a[2 * i + 1][0], a[2 * i + 1][2]);
-                    sts_v4(pbase + (uint32_t)((n0 + 8) >> 3) * 1024u + (uint32_t)r * 128u + chunk, a[2 * i][1],
-                           a[2 * i][3], a[2 * i + 1][1], a[2 * i + 1][3]);
-                }
-            }
+            const uint32_t rowbase = stage_b(s) + (uint32_t)(n >> 3) * 1024u + (uint32_t)(n & 7) * 128u;
+            store_chunks<BITS, GROUP, 0>(cw[buf], sbw[buf], rowbase, n & 7);
         };
         using B0 = std::integral_constant<int, 0>;
         using B1 = std::integral_constant<int, 1>;
@@ -333,8 +243,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             float* srow = p.slots + (size_t)slot * (P_TILE_M * P_TILE_N) + (size_t)m * P_TILE_N;
 #pragma unroll 1
             for (int cc = 0; cc < P_TILE_N / 32; ++cc) {
+                uint32_t vr[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(32 * cc), vr);
                 float v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(32 * cc), v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(vr[e]);
                 if (whole) {
                     if (m < M) {
                         for (int e = 0; e < 32; ++e) {
@@ -358,7 +271,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 __syncwarp();
                 unsigned prev = 0;
                 unsigned* ctr = &p.counters[(size_t)(P.ctr_begin + tile) * 4 + quarter];
-                if (lane == 0) prev = atom_add_acq_rel_p(ctr, 1u);
+                if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
                 __syncwarp();
                 prev = __shfl_sync(0xffffffffu, prev, 0);
                 const int t0 = tile * KB, t1 = t0 + KB - 1;
@@ -404,21 +317,33 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P_TMEM_COLS)
-                     : "memory");
+        tmem_dealloc(tmem, P_TMEM_COLS);
     }
 }
 
-template <int BITS>
-cudaError_t launch_prompt_bits(const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    prompt_kernel<BITS><<<grid, P_THREADS, prompt_smem_bytes(), st>>>(p, map);
+template <int BITS, int GROUP>
+cudaError_t launch_prompt_bg(const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
+    prompt_kernel<BITS, GROUP><<<grid, P_THREADS, prompt_smem_bytes(), st>>>(p, map);
     return cudaGetLastError();
 }
 
 template <int BITS>
-cudaError_t allow_prompt_bits() {
-    return cudaFuncSetAttribute(prompt_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)prompt_smem_bytes());
+cudaError_t launch_prompt_b(const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
+    if (p.group == 32) return launch_prompt_bg<BITS, 32>(p, map, grid, st);
+    if (p.group == 64) return launch_prompt_bg<BITS, 64>(p, map, grid, st);
+    return launch_prompt_bg<BITS, 128>(p, map, grid, st);
+}
+
+template <int BITS>
+cudaError_t allow_prompt_b() {
+    for (cudaError_t e : {cudaFuncSetAttribute(prompt_kernel<BITS, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)prompt_smem_bytes()),
+                          cudaFuncSetAttribute(prompt_kernel<BITS, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)prompt_smem_bytes()),
+                          cudaFuncSetAttribute(prompt_kernel<BITS, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)prompt_smem_bytes())})
+        if (e != cudaSuccess) return e;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -426,20 +351,20 @@ cudaError_t allow_prompt_bits() {
 size_t prompt_smem_bytes() { return (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PromptSmem) + 1024; }
 
 cudaError_t prompt_allow_smem() {
-    for (cudaError_t e : {allow_prompt_bits<2>(), allow_prompt_bits<3>(), allow_prompt_bits<4>(),
-                          allow_prompt_bits<5>(), allow_prompt_bits<6>(), allow_prompt_bits<8>()})
+    for (cudaError_t e : {allow_prompt_b<2>(), allow_prompt_b<3>(), allow_prompt_b<4>(), allow_prompt_b<5>(),
+                          allow_prompt_b<6>(), allow_prompt_b<8>()})
         if (e != cudaSuccess) return e;
     return cudaSuccess;
 }
 
 cudaError_t launch_prompt(int bits, const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
     switch (bits) {
-        case 2: return launch_prompt_bits<2>(p, map, grid, st);
-        case 3: return launch_prompt_bits<3>(p, map, grid, st);
-        case 4: return launch_prompt_bits<4>(p, map, grid, st);
-        case 5: return launch_prompt_bits<5>(p, map, grid, st);
-        case 6: return launch_prompt_bits<6>(p, map, grid, st);
-        case 8: return launch_prompt_bits<8>(p, map, grid, st);
+        case 2: return launch_prompt_b<2>(p, map, grid, st);
+        case 3: return launch_prompt_b<3>(p, map, grid, st);
+        case 4: return launch_prompt_b<4>(p, map, grid, st);
+        case 5: return launch_prompt_b<5>(p, map, grid, st);
+        case 6: return launch_prompt_b<6>(p, map, grid, st);
+        case 8: return launch_prompt_b<8>(p, map, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

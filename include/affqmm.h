@@ -89,7 +89,7 @@ AFFQMM_API const char* affqmm_strerror(int status);
 AFFQMM_API int affqmm_version(void);
 
 /* Bytes of packed storage for an N x K table (host call, no GPU needed).
- * Rows are padded to multiples of 16 and the depth to multiples of 128; the
+ * Rows are padded to multiples of 128 and the depth to multiples of 128; the
  * padding holds zero codes with zero scale and bias.
  * Errors: E_NULL (bytes), E_BITS, E_GROUP, E_SHAPE. */
 AFFQMM_API int affqmm_packed_bytes(int bits, int group, int64_t N, int64_t K, size_t* bytes);

@@ -53,9 +53,9 @@ def test_packed_bytes_closed_form(bits, group):
     for N, K in [(512, 256), (30720, 3840), (17, 96 if group == 32 else 2 * group), (1, group), (0, 0)]:
         if K % group:
             continue
-        tiles = -(-N // 16)
-        kb = -(-K // 128)
-        want = tiles * kb * (256 * bits + 8192 // group)
+        tiles = -(-N // 128)          # 128-row tiles
+        kb = -(-K // 128)             # 128-deep blocks
+        want = tiles * kb * (128 * 128 * bits // 8 + 128 * 4 * (128 // group))
         assert api.packed_bytes(bits, group, N, K) == want
 
 
