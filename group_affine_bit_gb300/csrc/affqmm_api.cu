@@ -32,11 +32,10 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_once[kMaxDevices];
 
-// Decode kernel shape: a ring of 4 stages (weight block + activation tile
-// each) and two CTAs per SM -- each CTA holds 256 of the SM's 512
-// tensor-memory columns.  That keeps 70-150 KB of weights in flight per SM.
-constexpr int kDecRing = 4;
-constexpr int kDecCtasPerSm = 2;
+// Decode kernel shape: one CTA per SM -- it holds all 512 tensor-memory
+// columns -- with a ring of up to 12 stages (weight block and activation
+// tile), 100-150 KB of weights in flight per SM.
+constexpr int kDecCtasPerSm = 1;
 
 int device_info(DeviceInfo** out) {
     int dev = 0;
@@ -95,7 +94,6 @@ int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, De
     p.KB = KB;
     p.K = K;
     p.M = (int32_t)M;
-    p.ring = kDecRing;
     const int64_t resident = (int64_t)d.sms * kDecCtasPerSm;
     int64_t ctas = 0, tiles_total = 0;
     for (int i = 0; i < count; ++i) {

@@ -28,15 +28,12 @@ struct DecProj {
     int32_t slot_begin;   // first partial slot (two per CTA)
 };
 
-constexpr int kDecMaxRing = 8;
-
 struct DecParams {
     DecProj proj[AFFQMM_MAX_STACK];
     int32_t nproj;
     int32_t KB;              // k-blocks of 128
     int64_t K;
     int32_t M;               // activation rows (1..16)
-    int32_t ring;            // shared-memory stages (<= kDecMaxRing)
     uint32_t* status;        // device status word (bit 0: a bounded wait gave up)
     uint32_t* counters;
     float* partials;         // slot = 128 rows x 16 floats
@@ -87,7 +84,7 @@ constexpr size_t kPromptSlotFloats = 128 * 256;
 
 // Launchers (decode.cu, prompt.cu, pack.cu).  They return the launch's error.
 // decode.cu: the tensor map describes x [M, K] bf16 with a 64 x 16 box.
-size_t decode_smem_bytes(int bits, int group, int ring);
+size_t decode_smem_bytes(int bits, int group);
 cudaError_t decode_allow_smem();
 cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st);
 constexpr int kDecodeSmemMax = 200 * 1024;

@@ -8,13 +8,19 @@
 //     scale/bias words) with one 1-D bulk copy each into a ring of shared-
 //     memory stages, together with the block's 16 x 128 activation tile (TMA,
 //     128-byte swizzle, rows past M read as zero);
-//   * four dequantization warps, one thread per weight row, read the row's
-//     codes back, round every weight once as bf16(fma(s, q, b))
-//     (affqmm_format.cuh) and store the row into tensor memory with
-//     tcgen05.st -- the A operand never touches shared memory;
-//   * one thread issues the MMAs (M = 128, N = 16, K = 16) and commits;
-//   * four epilogue warps drain the accumulator with tcgen05.ld at the end of
-//     each tile segment and store bf16 y (coalesced along n).
+//   * four lanes of work take blocks i = 0, 1, 2, 3 (mod 4) of the run; each
+//     has a group of four dequantization warps -- one thread per weight row
+//     reads the row's codes back, rounds every weight once as
+//     bf16(fma(s, q, b)) (affqmm_format.cuh) and stores the row into the
+//     lane's tensor-memory buffer with tcgen05.st, so the A operand never
+//     touches shared memory -- and an MMA warp that issues the block's MMAs
+//     (M = 128, N = 16, K = 16) into the lane's accumulator chain and
+//     commits (at N = 16 a single issuing thread cannot keep up);
+//   * the group that dequantized a tile segment's last block adds the four
+//     chains with tcgen05.ld and stores bf16 y (coalesced along n).
+// One CTA per SM owns all 512 tensor-memory columns.  Every barrier has one
+// owner per phase sequence (stage s always belongs to lane s mod 4), so no
+// parity wait can be satisfied by a phase one round too old.
 // Prior art: the "reg variant" lane projection of the "Gemma 4 12B on the
 // native Metal engine" page (4-bit groups in tensor-op registers, K split per
 // shape); unlike it, every weight is rounded to bf16 before the contraction,
@@ -22,7 +28,8 @@
 //
 // Work split: the projection's blocks, numbered tile-major, are cut into one
 // contiguous run per resident CTA ("stream-K").  A tile cut by run boundaries
-// gets one fp32 partial per run; the last CTA to arrive (an atomic counter per
+// gets one fp32 partial per run (its accumulator chains added first, in chain
+// order); the last CTA to arrive (an atomic counter per
 // tile and 32-row quarter, no waiting) adds them in run order and resets the
 // counter.  The cut depends only on the projection, M and the device, so the
 // same inputs give the same bits on every call, alone or stacked.  Every wait
@@ -40,21 +47,27 @@
 namespace affqmm {
 namespace {
 
-constexpr int D_THREADS = 10 * 32;  // producer, MMA, 4 dequant, 4 epilogue warps
-constexpr int D_EPI_WARP0 = 6;
-constexpr int D_MMA_N = 16;          // activation rows per MMA (M <= 16)
+constexpr int D_LANES = 4;            // (dequant group, MMA issuer, A buffer, chain) lanes of work
+constexpr int D_THREADS = (1 + D_LANES + 4 * D_LANES) * 32;  // producer, 4 issuers, 4 groups of 4 warps
+constexpr int D_ISSUER0 = 1;
+constexpr int D_DEQ_WARP0 = 1 + D_LANES;
+constexpr int D_MMA_N = 16;           // activation rows per MMA (M <= 16)
 constexpr uint32_t D_X_PANEL = D_MMA_N * 128;      // 16 rows x 64 k bf16, 2 KB
 constexpr uint32_t D_X_BYTES = 2 * D_X_PANEL;      // one 128-deep block of x
-constexpr uint32_t D_TMEM_COLS = 256;
+constexpr uint32_t D_TMEM_COLS = 512;
 constexpr uint32_t D_A_COLS = KBLK / 2;            // 64 columns: 128 bf16 per row
-constexpr uint32_t D_ACC_COL0 = 2 * D_A_COLS;      // two A buffers, then two accumulators
+constexpr uint32_t D_ACC_COL0 = D_LANES * D_A_COLS;
+// Accumulators: one chain per lane of work (its blocks of the segment), and
+// two segments' worth so the next segment starts while the last one is
+// drained: column D_ACC_COL0 + 16 * (D_LANES * segment buffer + chain).
 constexpr uint32_t D_IDESC = idesc_bf16_f32(128, D_MMA_N);
+constexpr int D_RING_MAX = 12;
 
 struct DecSmem {
-    uint64_t full[kDecMaxRing];
-    uint64_t empty[kDecMaxRing];
-    uint64_t a_full[2];
-    uint64_t a_empty[2];
+    uint64_t full[D_RING_MAX];
+    uint64_t empty[D_RING_MAX];
+    uint64_t a_full[D_LANES];
+    uint64_t a_empty[D_LANES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
@@ -65,17 +78,31 @@ template <int BITS, int GROUP>
 constexpr uint32_t dec_stage_bytes() {
     return (uint32_t)((block_bytes(BITS, GROUP) + 1023) / 1024 * 1024) + D_X_BYTES;  // codes, then x (1 KB aligned)
 }
+// Ring depth: a stage is refilled once the MMAs of its block are done, so the
+// ring takes as many stages as fit in ~200 KB, a multiple of the work lanes
+// (stage s always belongs to lane s mod 4: no barrier is waited on by two
+// threads that could be a phase apart).
+constexpr int dec_ring_for(uint32_t stage_bytes) {
+    return (int)(200u * 1024u / stage_bytes) / D_LANES * D_LANES > D_RING_MAX
+               ? D_RING_MAX
+               : (int)(200u * 1024u / stage_bytes) / D_LANES * D_LANES;
+}
+template <int BITS, int GROUP>
+constexpr int dec_ring() {
+    return dec_ring_for(dec_stage_bytes<BITS, GROUP>());
+}
 
 template <int BITS, int GROUP>
-__global__ void __launch_bounds__(D_THREADS, 2)
+__global__ void __launch_bounds__(D_THREADS, 1)
     decode_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int BB = block_bytes(BITS, GROUP);
     constexpr uint32_t STAGE = dec_stage_bytes<BITS, GROUP>();
     constexpr uint32_t X_OFF = STAGE - D_X_BYTES;
+    constexpr int NS = dec_ring<BITS, GROUP>();
+    static_assert(NS >= D_LANES && NS % D_LANES == 0, "ring depth");
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const int NS = p.ring;
     DecSmem* sh = reinterpret_cast<DecSmem*>(smem_raw + (base - raw) + (size_t)NS * STAGE);
     const uint32_t sh_addr = base + (uint32_t)NS * STAGE;
 #define BAR(field, i) (sh_addr + (uint32_t)offsetof(DecSmem, field) + 8u * (uint32_t)(i))
@@ -93,18 +120,20 @@ __global__ void __launch_bounds__(D_THREADS, 2)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(BAR(full, s), 1);
-            mbar_init(BAR(empty, s), 5);  // four dequant warps read the codes, the MMAs read x
+            mbar_init(BAR(empty, s), 5);  // the four warps of the block's group read the codes, its MMAs read x
+        }
+        for (int l = 0; l < D_LANES; ++l) {
+            mbar_init(BAR(a_full, l), 4);
+            mbar_init(BAR(a_empty, l), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(BAR(a_full, b), 4);
-            mbar_init(BAR(a_empty, b), 1);
-            mbar_init(BAR(acc_full, b), 1);
-            mbar_init(BAR(acc_empty, b), 4);
+            mbar_init(BAR(acc_full, b), D_LANES);  // every issuer commits at every segment end
+            mbar_init(BAR(acc_empty, b), 4);       // the four warps of the group draining it
         }
         sh->abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(sh_addr + (uint32_t)offsetof(DecSmem, tmem_base), D_TMEM_COLS);
+    if (warp == D_ISSUER0) tmem_alloc(sh_addr + (uint32_t)offsetof(DecSmem, tmem_base), D_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -133,66 +162,77 @@ __global__ void __launch_bounds__(D_THREADS, 2)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp < D_DEQ_WARP0) {
+        // ---------------------------------------------------------- MMA issuers
+        // Issuer e takes the blocks i = e (mod 4) of the run (the ones group e
+        // dequantizes into A buffer e) and accumulates them into chain e of
+        // the segment.  Every issuer waits for the segment's accumulators to
+        // be drained and commits at every segment end, so none runs a segment
+        // ahead of another.
         if (lane == 0) {
-            int s = 0, seg = 0;
-            uint32_t ph = 0;
+            const int e = warp - D_ISSUER0;
+            int seg = 0, seg_start = u0;
             int kb = u0 % KB;
             bool open = false;
             for (int u = u0, i = 0; u < u1; ++u, ++i) {
-                const int ab = i & 1;
-                const uint32_t aph = (uint32_t)((i >> 1) & 1);
+                const bool seg_end = (kb == KB - 1) || (u == u1 - 1);
                 const int db = seg & 1;
-                if (!open) {  // the accumulator must have been drained
-                    if (!wait_or_abort(BAR(acc_empty, db), (uint32_t)((seg >> 1) & 1) ^ 1u, abort_flag, p.status)) break;
+                if (!open) {
+                    if (!wait_or_abort(BAR(acc_empty, db), (uint32_t)((seg >> 1) & 1) ^ 1u, abort_flag, p.status))
+                        break;
                     open = true;
                 }
-                if (!wait_or_abort(BAR(full, s), ph, abort_flag, p.status)) break;
-                if (!wait_or_abort(BAR(a_full, ab), aph, abort_flag, p.status)) break;
-                tc_fence_after();
-                const bool first = (kb == 0) || (u == u0);
-                const uint32_t xs = base + (uint32_t)s * STAGE + X_OFF;
+                if ((i & (D_LANES - 1)) == e) {
+                    const int s = i % NS;
+                    const uint32_t ph = (uint32_t)((i / NS) & 1);
+                    const uint32_t aph = (uint32_t)((i / D_LANES) & 1);
+                    if (!wait_or_abort(BAR(full, s), ph, abort_flag, p.status)) break;
+                    if (!wait_or_abort(BAR(a_full, e), aph, abort_flag, p.status)) break;
+                    tc_fence_after();
+                    const int j = u - seg_start;  // block index within the segment
+                    const uint32_t dcol = tmem + D_ACC_COL0 + (uint32_t)(D_LANES * db + e) * D_MMA_N;
+                    const uint32_t acol = tmem + (uint32_t)e * D_A_COLS;
+                    const uint64_t bd0 = sw128_desc(base + (uint32_t)s * STAGE + X_OFF);
 #pragma unroll
-                for (int j = 0; j < KBLK / 16; ++j) {
-                    const uint64_t bd = sw128_desc(xs + (uint32_t)(j >> 2) * D_X_PANEL + (uint32_t)(j & 3) * 32u);
-                    umma_ts(tmem + D_ACC_COL0 + (uint32_t)db * D_MMA_N, tmem + (uint32_t)ab * D_A_COLS + 8u * j, bd,
-                            D_IDESC, (first && j == 0) ? 0u : 1u);
+                    for (int k = 0; k < KBLK / 16; ++k) {
+                        // +32 bytes per 16-deep step, +2 KB per 64-deep panel (descriptor units of 16 bytes)
+                        const uint64_t bd = bd0 + (uint64_t)((k >> 2) * (D_X_PANEL >> 4) + (k & 3) * 2);
+                        umma_ts(dcol, acol + 8u * k, bd, D_IDESC, (j < D_LANES && k == 0) ? 0u : 1u);
+                    }
+                    umma_commit(BAR(a_empty, e));
+                    umma_commit(BAR(empty, s));
                 }
-                umma_commit(BAR(a_empty, ab));
-                umma_commit(BAR(empty, s));
-                if (kb == KB - 1 || u == u1 - 1) {
-                    umma_commit(BAR(acc_full, db));
+                if (seg_end) {
+                    umma_commit(BAR(acc_full, db));  // this issuer's MMAs of the segment (maybe none)
                     ++seg;
                     open = false;
+                    seg_start = u + 1;
                 }
                 if (++kb == KB) kb = 0;
-                if (++s == NS) {
-                    s = 0;
-                    ph ^= 1u;
-                }
             }
         }
-    } else if (warp < D_EPI_WARP0) {
-        // ---------------------------------------------------------- dequantization
-        const int q = warp & 3;       // tensor-memory lanes 32q .. 32q + 31
-        const int n = 32 * q + lane;  // weight row of this thread within the tile
-        int s = 0;
-        uint32_t ph = 0;
-        for (int u = u0, i = 0; u < u1; ++u, ++i) {
-            const int ab = i & 1;
-            const uint32_t aph = (uint32_t)((i >> 1) & 1);
+    } else {
+        // ------------------------------------------ dequantization (+ epilogue)
+        const int g = (warp - D_DEQ_WARP0) >> 2;  // group: blocks i = g (mod 4)
+        const int q = warp & 3;                   // tensor-memory lanes 32q .. 32q + 31
+        const int n_in = 32 * q + lane;           // weight row of this thread within the tile
+        const int M = p.M;
+        const int tile0 = u0 / KB;
+        for (int u = u0 + g, i = g; u < u1; u += D_LANES, i += D_LANES) {
+            const int s = i % NS;
+            const uint32_t ph = (uint32_t)((i / NS) & 1);
+            const uint32_t aph = (uint32_t)((i / D_LANES) & 1);
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), ph, abort_flag, p.status))) break;
             const uint32_t st = base + (uint32_t)s * STAGE;
             uint32_t cw[4 * BITS];
-            load_row_codes_smem<BITS>(st, n, cw);
+            load_row_codes_smem<BITS>(st, n_in, cw);
             uint32_t sbw[sb_words(GROUP)];
-            load_row_sb_smem<GROUP>(st + sb_offset(BITS, GROUP, n), sbw);
+            load_row_sb_smem<GROUP>(st + sb_offset(BITS, GROUP, n_in), sbw);
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(empty, s));  // codes are in registers
-            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, ab), aph ^ 1u, abort_flag, p.status))) break;
+            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, g), aph ^ 1u, abort_flag, p.status))) break;
             tc_fence_after();
-            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * D_A_COLS;
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)g * D_A_COLS;
             {
                 uint32_t w[32];
                 weight_pairs<BITS, GROUP, 0, 32>(cw, sbw, w);
@@ -206,85 +246,82 @@ __global__ void __launch_bounds__(D_THREADS, 2)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(a_full, ab));
-            if (++s == NS) {
-                s = 0;
-                ph ^= 1u;
-            }
-        }
-    } else {
-        // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;
-        const int n_in = 32 * q + lane;
-        const int M = p.M;
-        int seg = 0;
-        int seg_start = u0;
-        int kb = u0 % KB;
-        for (int u = u0; u < u1; ++u) {
-            const bool seg_end = (kb == KB - 1) || (u == u1 - 1);
-            const bool tile_end = kb == KB - 1;
-            if (++kb == KB) kb = 0;
-            if (!seg_end) continue;
+            if (lane == 0) mbar_arrive(BAR(a_full, g));
+
+            // ---- this block ends a tile segment: drain the accumulators
             const int tile = u / KB;
+            const int kb = u - tile * KB;
+            if (!(kb == KB - 1 || u == u1 - 1)) continue;
+            const int seg = tile - tile0;
             const int db = seg & 1;
+            const int seg_start = seg == 0 ? u0 : tile * KB;  // first block of the segment
+            const int len = u - seg_start + 1;
+            const int i_start = seg_start - u0;
             if (!__all_sync(0xffffffffu,
                             wait_or_abort(BAR(acc_full, db), (uint32_t)((seg >> 1) & 1), abort_flag, p.status)))
                 break;
             tc_fence_after();
-            uint32_t r[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + D_ACC_COL0 + (uint32_t)db * D_MMA_N, r);
+            // chain l holds the segment's blocks with run index = l (mod 4);
+            // add the chains that received a block, in chain order
+            float v[D_MMA_N];
+            bool any = false;
+            const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + D_ACC_COL0 + (uint32_t)(D_LANES * db) * D_MMA_N;
+#pragma unroll
+            for (int l = 0; l < D_LANES; ++l) {
+                const bool used = len >= D_LANES || ((l - i_start) & (D_LANES - 1)) < len;
+                uint32_t r[16];
+                tmem_ld16(trow + (uint32_t)l * D_MMA_N, r);
+                if (used) {
+#pragma unroll
+                    for (int e2 = 0; e2 < D_MMA_N; ++e2) v[e2] = any ? v[e2] + __uint_as_float(r[e2]) : __uint_as_float(r[e2]);
+                    any = true;
+                }
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(acc_empty, db));  // accumulator drained
+            if (lane == 0) mbar_arrive(BAR(acc_empty, db));  // accumulators drained
             const int64_t n = (int64_t)tile * TILE_N + n_in;
-            const bool whole = (seg_start == tile * KB) && tile_end;
+            const bool whole = (seg_start == tile * KB) && (kb == KB - 1);
             if (whole) {
                 if (n < P.N)
                     for (int m = 0; m < M; ++m)
-                        P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[m])));
-            } else {
-                // publish this run's partial of the tile; the last run to
-                // arrive adds them all in run (k) order
-                const int slot = P.slot_begin + 2 * c + (seg_start == u0 ? 0 : 1);
-                float4* sp = reinterpret_cast<float4*>(p.partials + ((size_t)slot * TILE_N + n_in) * D_MMA_N);
+                        P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v[m]));
+                continue;
+            }
+            // publish this run's partial of the tile; the last run to arrive
+            // adds them all in run (k) order
+            const int slot = P.slot_begin + 2 * c + (seg_start == u0 ? 0 : 1);
+            float4* sp = reinterpret_cast<float4*>(p.partials + ((size_t)slot * TILE_N + n_in) * D_MMA_N);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    __stcg(sp + e, make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                               __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])));
-                __syncwarp();
-                unsigned prev = 0;
-                unsigned* ctr = &p.counters[(size_t)(P.ctr_begin + tile) * 4 + q];
-                if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
-                __syncwarp();
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                const int t0 = tile * KB, t1 = t0 + KB - 1;
-                const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
-                if (prev == (unsigned)(cl - cf)) {
-                    float acc[D_MMA_N];
+            for (int e2 = 0; e2 < 4; ++e2) __stcg(sp + e2, make_float4(v[4 * e2], v[4 * e2 + 1], v[4 * e2 + 2], v[4 * e2 + 3]));
+            __syncwarp();
+            unsigned prev = 0;
+            unsigned* ctr = &p.counters[(size_t)(P.ctr_begin + tile) * 4 + q];
+            if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
+            __syncwarp();
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            const int t0 = tile * KB, t1 = t0 + KB - 1;
+            const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
+            if (prev != (unsigned)(cl - cf)) continue;
+            float acc[D_MMA_N];
 #pragma unroll
-                    for (int e = 0; e < D_MMA_N; ++e) acc[e] = 0.f;
-                    for (int cb = cf; cb <= cl; ++cb) {
-                        const int b0 = (int)((int64_t)cb * U / PC);
-                        const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
-                        const float4* cp =
-                            reinterpret_cast<const float4*>(p.partials + ((size_t)sc * TILE_N + n_in) * D_MMA_N);
+            for (int e2 = 0; e2 < D_MMA_N; ++e2) acc[e2] = 0.f;
+            for (int cb = cf; cb <= cl; ++cb) {
+                const int b0 = (int)((int64_t)cb * U / PC);
+                const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
+                const float4* cp = reinterpret_cast<const float4*>(p.partials + ((size_t)sc * TILE_N + n_in) * D_MMA_N);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 f = __ldcg(cp + e);
-                            acc[4 * e] += f.x;
-                            acc[4 * e + 1] += f.y;
-                            acc[4 * e + 2] += f.z;
-                            acc[4 * e + 3] += f.w;
-                        }
-                    }
-                    if (n < P.N)
-                        for (int m = 0; m < M; ++m)
-                            P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
-                    if (lane == 0) *ctr = 0u;
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const float4 f = __ldcg(cp + e2);
+                    acc[4 * e2] += f.x;
+                    acc[4 * e2 + 1] += f.y;
+                    acc[4 * e2 + 2] += f.z;
+                    acc[4 * e2 + 3] += f.w;
                 }
             }
-            ++seg;
-            seg_start = u + 1;
+            if (n < P.N)
+                for (int m = 0; m < M; ++m) P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+            if (lane == 0) *ctr = 0u;
         }
     }
 #undef BAR
@@ -292,7 +329,7 @@ __global__ void __launch_bounds__(D_THREADS, 2)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == D_ISSUER0) {
         tc_fence_after();
         tmem_dealloc(tmem, D_TMEM_COLS);
     }
@@ -300,7 +337,7 @@ __global__ void __launch_bounds__(D_THREADS, 2)
 
 template <int BITS, int GROUP>
 cudaError_t launch_bg(const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    const size_t smem = (size_t)p.ring * dec_stage_bytes<BITS, GROUP>() + sizeof(DecSmem) + 1024;
+    const size_t smem = (size_t)dec_ring<BITS, GROUP>() * dec_stage_bytes<BITS, GROUP>() + sizeof(DecSmem) + 1024;
     decode_kernel<BITS, GROUP><<<grid, D_THREADS, smem, st>>>(p, map);
     return cudaGetLastError();
 }
@@ -327,9 +364,9 @@ cudaError_t allow_b() {
 
 }  // namespace
 
-size_t decode_smem_bytes(int bits, int group, int ring) {
+size_t decode_smem_bytes(int bits, int group) {
     const size_t stage = (size_t)(block_bytes(bits, group) + 1023) / 1024 * 1024 + D_X_BYTES;
-    return (size_t)ring * stage + sizeof(DecSmem) + 1024;
+    return (size_t)dec_ring_for((uint32_t)stage) * stage + sizeof(DecSmem) + 1024;
 }
 
 cudaError_t decode_allow_smem() {
