@@ -50,7 +50,7 @@ KERNEL_SOURCES = ["group_affine_bit_gb300/csrc/decode.cu", "group_affine_bit_gb3
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: per workload)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="gate_up_decode",
                     choices=["gate_up_decode", "decode_step", "prompt_chunk", "lane_sweep", "tiny"])
@@ -186,23 +186,33 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workloads
-class Projection:
-    """One resident projection with `copies` rotating weight copies."""
+def copies_for(bytes_per_copy: int) -> int:
+    """Rotating copies so that more than twice the L2 is touched between two
+    reads of one copy."""
+    return max(4, math.ceil(2 * L2_BYTES / max(1, bytes_per_copy)))
 
-    def __init__(self, api, synth, bits, group, M, N, K, seed, copies, device):
+
+class Case:
+    """One resident projection: `copies` packed copies of one seeded affine
+    table (the same values), its activations and its output."""
+
+    def __init__(self, api, synth, label, bits, group, M, N, K, seed, copies, device):
         import torch
-        self.bits, self.group, self.M, self.N, self.K = bits, group, M, N, K
+        self.api = api
+        self.label, self.bits, self.group, self.M, self.N, self.K, self.seed = label, bits, group, M, N, K, seed
+        self.copies = copies
         g = synth.generator(seed, device)
-        self.ws = []
-        for _ in range(copies):
-            codes, s, b = synth.affine_table(bits, group, N, K, g, device)
-            self.ws.append(api.pack(codes, s, b, bits, group))
-            del codes, s, b
+        codes, s, b = synth.affine_table(bits, group, N, K, g, device)
+        self.ws = [api.pack(codes, s, b, bits, group) for _ in range(copies)]
+        del codes, s, b
         self.x = synth.activations(M, K, g, device)
         self.y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
 
+    def run(self, i: int, workspace):
+        self.api.run(self.ws[i % self.copies], self.x, y=self.y, workspace=workspace)
+
     @property
-    def packed_bytes(self) -> int:
+    def packed_bytes(self) -> int:   # codes + bf16 scale and bias per group
         return self.N * self.K * self.bits // 8 + 4 * self.N * self.K // self.group
 
     @property
@@ -213,59 +223,173 @@ class Projection:
     def flops(self) -> int:
         return 2 * self.M * self.N * self.K
 
+    @property
+    def launches(self) -> int:
+        return 1 if self.M <= 16 else -(-self.M // 128)
 
-def copies_for(bytes_per_copy: int) -> int:
-    return max(4, math.ceil(2 * L2_BYTES / max(1, bytes_per_copy)))
+    def oracle_shape(self):
+        return dict(bits=self.bits, group=self.group, M=self.M, N=self.N, K=self.K, seed=self.seed)
 
 
-class GateUpDecode:
-    name = "gate_up_decode"
+class Workload:
+    """A step = every case run once, in order, on one stream."""
+    name = ""
     unit = "GB/s"
+    default_steps = 3000
 
-    def __init__(self, api, synth, device, shape=None):
-        c = shape or synth.GATE_UP_DECODE
-        self.cfg = dict(c)
-        one = c["N"] * c["K"] * c["bits"] // 8 + 4 * c["N"] * c["K"] // c["group"]
-        self.copies = copies_for(one)
-        self.p = Projection(api, synth, c["bits"], c["group"], c["M"], c["N"], c["K"], c["seed"], self.copies, device)
+    def __init__(self, api, synth, device):
         self.api = api
-        self.ws = api.Workspace(device)
+        self.workspace = api.Workspace(device)
+        self.cases = self.make_cases(api, synth, device)
+
+    def make_cases(self, api, synth, device):
+        raise NotImplementedError
 
     def step(self, i: int):
-        self.api.run(self.p.ws[i % self.copies], self.p.x, y=self.p.y, workspace=self.ws)
+        for c in self.cases:
+            c.run(i, self.workspace)
 
-    launches_per_step = 1
-    units_per_step = property(lambda self: self.p.packed_bytes)
+    @property
+    def launches_per_step(self) -> int:
+        return sum(c.launches for c in self.cases)
+
+    @property
+    def units_per_step(self) -> float:
+        """Units of the metric: packed-weight bytes, or FLOPs for prompt rows."""
+        if self.unit == "TFLOP/s":
+            return float(sum(c.flops for c in self.cases))
+        return float(sum(c.packed_bytes for c in self.cases))
+
+    @property
+    def scale(self) -> float:
+        return 1e12 if self.unit == "TFLOP/s" else 1e9
 
     def roofline_info(self):
-        return dict(kernel=f"decode_kernel<{self.p.bits},{1 if self.p.M <= 8 else 2}>", bound="hbm",
-                    units_per_launch=self.p.algorithmic_bytes, launches_per_step=1,
-                    traffic_key=f"decode {self.name} M{self.p.M}")
+        c0 = self.cases[0]
+        if self.unit == "TFLOP/s":
+            return dict(kernel=f"prompt_kernel<{c0.bits},{c0.group}>", bound="tensor",
+                        units_per_step=float(sum(c.flops for c in self.cases)), unit="TFLOP/s",
+                        traffic_key=f"prompt {self.name}")
+        return dict(kernel=f"decode_kernel<{c0.bits},{c0.group}>", bound="hbm",
+                    units_per_step=float(sum(c.algorithmic_bytes for c in self.cases)), unit="GB/s",
+                    traffic_key=f"decode {self.name}")
+
+    def l2_note(self) -> str:
+        touched = sum(c.packed_bytes for c in self.cases)
+        rot = max(c.copies for c in self.cases)
+        if rot > 1:
+            return (f"inputs larger than L2: {rot} rotating weight copies per case "
+                    f"({rot * touched / 1e6:.0f} MB touched per rotation > 129 MB L2)")
+        return f"inputs larger than L2: {touched / 1e6:.0f} MB of distinct packed weights per step > 129 MB L2"
+
+    def describe(self) -> str:
+        return self.name
 
     def config(self):
-        c = self.cfg
-        return {"workload": f"{self.name}: M={c['M']} K={c['K']} N={c['N']} {c['bits']}-bit group {c['group']}",
-                "M": c["M"], "K": c["K"], "N": c["N"], "bits": c["bits"], "group": c["group"], "seed": c["seed"],
-                "l2": f"inputs larger than L2: {self.copies} rotating weight copies "
-                      f"({self.copies * self.p.packed_bytes / 1e6:.0f} MB > 129 MB L2)",
-                "parallelism": "replicas"}
+        return {"workload": self.describe(), "cases": [
+            f"{c.label}: M={c.M} N={c.N} K={c.K} {c.bits}-bit g{c.group} seed {c.seed}" for c in self.cases],
+            "l2": self.l2_note(), "parallelism": "replicas"}
 
-    # host-side I/O of one step for the end-to-end timing
     def e2e_io(self):
-        return [self.p.x], [self.p.y]
+        return [c.x for c in self.cases], [c.y for c in self.cases]
 
-    def oracle_problem(self):
-        return [(self.cfg["bits"], self.cfg["group"], self.cfg["M"], self.cfg["N"], self.cfg["K"], self.cfg["seed"])]
+    def oracle_shape(self):
+        return self.cases[0].oracle_shape()
+
+
+class GateUpDecode(Workload):
+    name = "gate_up_decode"
+
+    def make_cases(self, api, synth, device, shape=None):
+        c = shape or synth.GATE_UP_DECODE
+        one = c["N"] * c["K"] * c["bits"] // 8 + 4 * c["N"] * c["K"] // c["group"]
+        return [Case(api, synth, self.name, c["bits"], c["group"], c["M"], c["N"], c["K"], c["seed"],
+                     copies_for(one), device)]
+
+    def describe(self):
+        c = self.cases[0]
+        return f"{self.name}: M={c.M} K={c.K} N={c.N} {c.bits}-bit group {c.group}"
 
 
 class Tiny(GateUpDecode):
     name = "tiny"
 
-    def __init__(self, api, synth, device):
-        super().__init__(api, synth, device, synth.TINY)
+    def make_cases(self, api, synth, device):
+        return super().make_cases(api, synth, device, synth.TINY)
 
 
-WORKLOADS = {"gate_up_decode": GateUpDecode, "tiny": Tiny}
+class DecodeStep(Workload):
+    """A 60-layer decoder's projections (qkv, o, gate/up, down) and the tied
+    head, M = 1: every weight distinct, about 16 GB read per step."""
+    name = "decode_step"
+    default_steps = 200
+
+    def make_cases(self, api, synth, device):
+        bits, group, seed = 4, 64, synth.DECODE_STEP_SEED
+        cases = []
+        for layer in range(synth.N_LAYERS):
+            for j, (label, (N, K)) in enumerate(synth.DECODER_LAYER_SHAPES.items()):
+                cases.append(Case(api, synth, f"L{layer}.{label}", bits, group, 1, N, K,
+                                  synth.step_seed(seed, layer, j), 1, device))
+        N, K = synth.HEAD_SHAPE
+        cases.append(Case(api, synth, "head", bits, group, 1, N, K, synth.step_seed(seed, synth.N_LAYERS, 0), 1,
+                          device))
+        return cases
+
+    def describe(self):
+        return (f"{self.name}: {synth_n_layers(self)} layers x (qkv, o, gate_up, down) + tied head, M=1, "
+                f"hidden 5376, 4-bit group 64, {len(self.cases)} projections")
+
+    def config(self):
+        d = super().config()
+        d["cases"] = d["cases"][:4] + [d["cases"][-1], f"... {len(self.cases)} projections in all"]
+        d["packed_gb_per_step"] = round(self.units_per_step / 1e9, 3)
+        return d
+
+    def oracle_shape(self):
+        return self.cases[2].oracle_shape()   # a gate/up projection
+
+
+def synth_n_layers(wl) -> int:
+    return (len(wl.cases) - 1) // 4
+
+
+class PromptChunk(Workload):
+    """M = 128 activation rows through one decoder layer's four projections."""
+    name = "prompt_chunk"
+    unit = "TFLOP/s"
+    default_steps = 500
+
+    def make_cases(self, api, synth, device):
+        c = synth.PROMPT_CHUNK
+        return [Case(api, synth, label, c["bits"], c["group"], c["M"], N, K, synth.step_seed(c["seed"], 0, j), 1,
+                     device) for j, (label, (N, K)) in enumerate(synth.DECODER_LAYER_SHAPES.items())]
+
+    def describe(self):
+        return f"{self.name}: M=128 through qkv, o, gate_up, down (hidden 5376), 4-bit group 64"
+
+
+class LaneSweep(Workload):
+    """M in {2, 4, 8, 16} at 4-bit g64 and M = 16 at 8-bit g32, 3-bit g64 and
+    2-bit g128 on K = 3840, N = 15360."""
+    name = "lane_sweep"
+    default_steps = 1000
+
+    def make_cases(self, api, synth, device):
+        c = synth.SWEEP_SHAPE
+        out = []
+        for j, (M, bits, group) in enumerate(synth.SWEEP_CASES):
+            one = c["N"] * c["K"] * bits // 8 + 4 * c["N"] * c["K"] // group
+            out.append(Case(api, synth, f"M{M} {bits}b g{group}", bits, group, M, c["N"], c["K"], c["seed"] + j,
+                            copies_for(one), device))
+        return out
+
+    def describe(self):
+        return f"{self.name}: K=3840 N=15360, (M, bits, group) in {[(c.M, c.bits, c.group) for c in self.cases]}"
+
+
+WORKLOADS = {"gate_up_decode": GateUpDecode, "decode_step": DecodeStep, "prompt_chunk": PromptChunk,
+             "lane_sweep": LaneSweep, "tiny": Tiny}
 
 
 # ----------------------------------------------------------------------------- timing
@@ -279,7 +403,8 @@ def graph_of(fn, first: int, count: int):
 
 
 def time_steps(wl, steps: int, warmup: int, dist, device):
-    """Device time of exactly `steps` steps replayed from CUDA graphs."""
+    """Device time of exactly `steps` steps replayed from CUDA graphs (at most
+    about 2000 launches per graph)."""
     import torch
     side = torch.cuda.Stream(device)
     side.wait_stream(torch.cuda.current_stream(device))
@@ -288,7 +413,7 @@ def time_steps(wl, steps: int, warmup: int, dist, device):
             wl.step(i)
     torch.cuda.current_stream(device).wait_stream(side)
     torch.cuda.synchronize(device)
-    chunk = min(steps, 500)
+    chunk = max(1, min(steps, 2000 // max(1, wl.launches_per_step)))
     full = graph_of(wl.step, 0, chunk)
     rest = graph_of(wl.step, 0, steps % chunk) if steps % chunk else None
     for _ in range(max(1, warmup // chunk)):
@@ -322,7 +447,7 @@ def sustain_for_clocks(graphs, device, seconds: float = 1.0):
         torch.cuda.synchronize(device)
 
 
-def time_e2e(wl, api, steps: int, device):
+def time_e2e(wl, steps: int, device):
     """Same steps through the Python API, activations uploaded from pinned host
     memory and outputs read back to pinned host memory every step."""
     import torch
@@ -354,14 +479,15 @@ def time_e2e(wl, api, steps: int, device):
 # ----------------------------------------------------------------------------- oracle
 class OracleSample:
     """The CPU oracle on a bounded sample of a workload: whole output rows of
-    the same projection (same seed, same values), threaded over rows on all
-    host cores.  Rate = packed-weight bytes of the sampled rows per second."""
+    one of its projections (same seed, same values), threaded over rows on
+    all host cores.  Rate = packed-weight bytes (GB/s) or FLOPs (TFLOP/s) of
+    the sampled rows per second."""
 
-    def __init__(self, wl_name: str):
+    def __init__(self, shape: dict, unit: str):
         import oracle
         from group_affine_bit_gb300 import synth
         self.orc = oracle.load()
-        shape = synth.TINY if wl_name == "tiny" else synth.GATE_UP_DECODE
+        self.unit = unit
         self.bits, self.group = shape["bits"], shape["group"]
         self.M, self.N, self.K = shape["M"], shape["N"], shape["K"]
         x, codes, s, b = synth.problem(self.bits, self.group, self.M, self.N, self.K, shape["seed"])
@@ -369,8 +495,10 @@ class OracleSample:
         self.sb, self.bb = synth.bits_u16(s), synth.bits_u16(b)
         self.threads = host_cores()
 
-    def row_bytes(self, rows: int) -> int:
-        return rows * self.K * self.bits // 8 + 4 * rows * self.K // self.group
+    def units(self, rows: int) -> float:
+        if self.unit == "TFLOP/s":
+            return 2.0 * self.M * rows * self.K / 1e12
+        return (rows * self.K * self.bits // 8 + 4 * rows * self.K // self.group) / 1e9
 
     def run(self, rows: int) -> float:
         t0 = time.perf_counter()
@@ -384,8 +512,8 @@ class OracleSample:
         return int(max(1, min(self.N, n * seconds / dt)))
 
     def describe(self, rows: int, reps: int) -> str:
-        return (f"{reps} x {rows} of {self.N} output rows of the same projection (M={self.M}, K={self.K}, "
-                f"{self.bits}-bit g{self.group}); float64 oracle threaded over rows")
+        return (f"{reps} x {rows} of {self.N} output rows of one projection of the workload (M={self.M}, "
+                f"K={self.K}, {self.bits}-bit g{self.group}); float64 oracle threaded over rows")
 
     def rate(self, seconds: float):
         rows = self.rows_for(seconds)
@@ -393,7 +521,23 @@ class OracleSample:
         while total < seconds or reps == 0:
             total += self.run(rows)
             reps += 1
-        return self.row_bytes(rows) * reps / total / 1e9, self.describe(rows, reps), total
+        return self.units(rows) * reps / total, self.describe(rows, reps), total
+
+
+WORKLOAD_ORACLE_SHAPES = {   # the projection each workload's oracle sample takes rows of
+    "gate_up_decode": lambda s: s.GATE_UP_DECODE,
+    "tiny": lambda s: s.TINY,
+    "decode_step": lambda s: dict(bits=4, group=64, M=1, N=s.DECODER_LAYER_SHAPES["gate_up"][0],
+                                  K=s.DECODER_LAYER_SHAPES["gate_up"][1], seed=s.step_seed(s.DECODE_STEP_SEED, 0, 2)),
+    "prompt_chunk": lambda s: dict(bits=4, group=64, M=128, N=s.DECODER_LAYER_SHAPES["qkv"][0],
+                                   K=s.DECODER_LAYER_SHAPES["qkv"][1], seed=s.step_seed(s.PROMPT_CHUNK["seed"], 0, 0)),
+    "lane_sweep": lambda s: dict(bits=4, group=64, M=2, N=s.SWEEP_SHAPE["N"], K=s.SWEEP_SHAPE["K"],
+                                 seed=s.SWEEP_SHAPE["seed"]),
+}
+
+
+def workload_unit(name: str) -> str:
+    return WORKLOADS[name].unit
 
 
 # ----------------------------------------------------------------------------- main
@@ -402,23 +546,26 @@ def run_reference(args, rank, world):
     bounded sample of the workload."""
     if rank != 0:
         return 0
-    smp = OracleSample(args.workload)
-    per_step = max(0.02, args.cpu_seconds / max(1, args.steps + args.warmup))
+    from group_affine_bit_gb300 import synth
+    unit = workload_unit(args.workload)
+    steps = args.steps if args.steps is not None else 20
+    smp = OracleSample(WORKLOAD_ORACLE_SHAPES[args.workload](synth), unit)
+    per_step = max(0.02, args.cpu_seconds / max(1, steps + args.warmup))
     rows = smp.rows_for(per_step)
     for _ in range(args.warmup):
         smp.run(rows)
     total = 0.0
-    for _ in range(args.steps):
+    for _ in range(steps):
         total += smp.run(rows)
-    value = smp.row_bytes(rows) * args.steps / total / 1e9
+    value = smp.units(rows) * steps / total
     sample = smp.describe(rows, 1) + " per step"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / max(1, args.steps) * 1e3,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": 1,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": total / max(1, steps) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": args.workload, "sample": sample},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": smp.threads, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": unit, "cores": smp.threads, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -442,51 +589,61 @@ def main(argv=None):
     api.lib()
 
     wl = WORKLOADS[args.workload](api, synth, device)
+    steps = args.steps if args.steps is not None else wl.default_steps
     warmup = max(3, args.warmup)
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-    seconds, graphs = time_steps(wl, args.steps, warmup, dist, device)
+    seconds, graphs = time_steps(wl, steps, warmup, dist, device)
+    clocks = None
     if sampler:
         if seconds < 1.0:
             sustain_for_clocks(graphs, device, 1.0)
         clocks = sampler.stop()
     t_max = reduce_max(dist, seconds, device)
-    units = wl.units_per_step * args.steps
-    value = aggregate(units, world, t_max) / 1e9
+    value = aggregate(wl.units_per_step * steps, world, t_max) / wl.scale
 
     info = wl.roofline_info()
     peaks = measured_peaks()
-    achieved = info["units_per_launch"] / (seconds / (args.steps * info["launches_per_step"])) / 1e9
-    roofline = {"bound": info["bound"], "kernel": info["kernel"], "achieved": achieved,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "peak_source": f"{peaks['source']} hbm_gbs (copy)",
+    launches = steps * wl.launches_per_step
+    per_launch_s = seconds / launches
+    units_per_launch = info["units_per_step"] / wl.launches_per_step
+    if info["bound"] == "hbm":
+        achieved = units_per_launch / per_launch_s / 1e9
+        peak, peak_name = peaks["hbm_gbs"], "hbm_gbs (copy)"
+    else:
+        achieved = units_per_launch / per_launch_s / 1e12
+        sustained = seconds >= 1.0
+        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        peak_name = "bf16_tflops_sustained (cuBLAS)" if sustained else "bf16_tflops burst (cuBLAS)"
+    roofline = {"bound": info["bound"], "kernel": info["kernel"], "achieved": achieved, "peak": peak,
+                "unit": info["unit"], "frac": achieved / peak, "peak_source": f"{peaks['source']} {peak_name}",
                 "traffic": committed_traffic(info["traffic_key"]),
-                "bytes_per_launch": info["units_per_launch"]}
+                ("bytes_per_launch" if info["bound"] == "hbm" else "flop_per_launch"): units_per_launch,
+                "launch_us": per_launch_s * 1e6}
 
     e2e = None
     if not args.no_e2e:
-        e2e_steps = min(args.steps, 2000)
-        t_e2e, bi, bo = time_e2e(wl, api, e2e_steps, device)
+        e2e_steps = min(steps, 2000)
+        t_e2e, bi, bo = time_e2e(wl, e2e_steps, device)
         t_e2e = reduce_max(dist, t_e2e, device)
-        e2e = {"value": aggregate(wl.units_per_step * e2e_steps, world, t_e2e) / 1e9, "unit": "GB/s",
+        e2e = {"value": aggregate(wl.units_per_step * e2e_steps, world, t_e2e) / wl.scale, "unit": wl.unit,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        smp = OracleSample(args.workload)
+        smp = OracleSample(WORKLOAD_ORACLE_SHAPES[args.workload](synth), wl.unit)
         r, sample, dt = smp.rate(args.cpu_seconds)
-        cpu = {"value": r, "unit": "GB/s", "cores": smp.threads, "kind": "oracle", "sample": sample,
+        cpu = {"value": r, "unit": wl.unit, "cores": smp.threads, "kind": "oracle", "sample": sample,
                "seconds": round(dt, 2)}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-                "warmup": warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+        line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world, "steps": steps,
+                "warmup": warmup, "ms_per_step": t_max / steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": wl.config(), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps * wl.launches_per_step, "clocks": clocks,
-                "kernel_src_digest": source_digest()}
+                "gpu_launches": launches, "clocks": clocks, "kernel_src_digest": source_digest()}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
