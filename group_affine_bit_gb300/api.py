@@ -19,12 +19,14 @@ LIB_PATH = os.path.join(_PKG, "libaffqmm.so")
 
 MAX_STACK = 8
 MAX_M = 1 << 20
+NOALLOC_MAX_M = 16                   # rows affqmm_run_noalloc takes
 WORKSPACE_ZEROED = 256 + 65536 * 4   # leading workspace bytes kept zero between calls
 
 STATUS_NAMES = {
     0: "AFFQMM_OK", 1: "AFFQMM_E_NULL", 2: "AFFQMM_E_BITS", 3: "AFFQMM_E_GROUP",
     4: "AFFQMM_E_SHAPE", 5: "AFFQMM_E_ALIGN", 6: "AFFQMM_E_M", 7: "AFFQMM_E_WORKSPACE",
     8: "AFFQMM_E_TIMEOUT", 9: "AFFQMM_E_CUDA", 10: "AFFQMM_E_ARG", 11: "AFFQMM_E_DEVICE",
+    12: "AFFQMM_E_SCRATCH",
 }
 
 
@@ -63,6 +65,7 @@ def lib() -> ctypes.CDLL:
             "affqmm_run_stacked": (i32, [i32, wp, vp, i64, ctypes.POINTER(vp), vp, ctypes.c_size_t, vp]),
             "affqmm_dequant": (i32, [wp, vp, vp]),
             "affqmm_workspace_status": (i32, [vp, vp]),
+            "affqmm_run_noalloc": (i32, [wp, vp, i64, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -217,3 +220,19 @@ def dequant(w: PackedWeight, stream=None) -> torch.Tensor:
 def workspace_status(buf: torch.Tensor, stream=None) -> int:
     """Read and clear a workspace's device status word (0 = ok)."""
     return int(lib().affqmm_workspace_status(buf.data_ptr(), _stream_ptr(stream)))
+
+
+def run_noalloc(w: PackedWeight, x: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Tensor:
+    """affqmm_run_noalloc: y = bf16(x @ dequant(W)^T) for M <= 16 rows, with no
+    workspace.  For callers that cannot allocate device memory; the library
+    works in its own fixed 3 MiB scratch array instead, shared by every call on
+    the device, so calls must not overlap on the GPU.  `y` must be given: this
+    wrapper allocates nothing either."""
+    _check_x(x, w.K)
+    M = x.shape[0]
+    if y.dtype != torch.bfloat16 or tuple(y.shape) != (M, w.N) or not y.is_contiguous() or y.device != x.device:
+        raise ValueError(f"y must be a contiguous bf16 [{M}, {w.N}] tensor on {x.device}")
+    cw = w.cstruct()
+    _check(lib().affqmm_run_noalloc(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), _stream_ptr(stream)),
+           "affqmm_run_noalloc")
+    return y

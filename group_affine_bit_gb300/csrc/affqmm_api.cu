@@ -320,6 +320,8 @@ const char* affqmm_strerror(int status) {
         case AFFQMM_E_CUDA: return "a CUDA call or launch failed";
         case AFFQMM_E_ARG: return "bad argument (count or mismatched stacked weights)";
         case AFFQMM_E_DEVICE: return "the current device is not an sm_103 GPU";
+        case AFFQMM_E_SCRATCH:
+            return "affqmm_run_noalloc: M > 16, or the work needs more than its 3 MiB built-in scratch";
         default: return "unknown affqmm status";
     }
 }
@@ -403,3 +405,85 @@ int affqmm_workspace_status(void* workspace, void* stream) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// affqmm_run_noalloc: the decode path (M <= 16) for callers that cannot
+// allocate device memory -- a plug-in inside a host engine that owns all of
+// the GPU's memory and gives it no allocator, or a latency-critical loop that
+// must not call cudaMalloc/cudaFree (which can synchronize the device).  Its
+// scratch (status word, merge counters, split-depth partial sums, in the
+// workspace layout of affqmm_run) is the file-scope array below, which every
+// GPU that loads this library holds until the process exits.  Calls share it:
+// calls that overlap on the GPU race on it.
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[AFFQMM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// In host code `g_noalloc_scratch` names a host-side stand-in, not device
+// memory: kernels get the address that cudaGetSymbolAddress returns for the
+// current device, looked up once per device.
+struct NoallocScratch {
+    void* ptr = nullptr;
+    bool ok = false;
+};
+NoallocScratch g_noalloc[kMaxDevices];
+std::once_flag g_noalloc_once[kMaxDevices];
+
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AFFQMM_E_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return AFFQMM_E_DEVICE;
+    std::call_once(g_noalloc_once[dev], [dev] {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return;
+        g_noalloc[dev].ptr = p;
+        g_noalloc[dev].ok = true;
+    });
+    if (!g_noalloc[dev].ok) return AFFQMM_E_CUDA;
+    *out = g_noalloc[dev].ptr;
+    return AFFQMM_OK;
+}
+
+}  // namespace
+
+extern "C" int affqmm_run_noalloc(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y,
+                                  void* stream) {
+    int rc = check_weight(w);
+    if (rc) return rc;
+    if (M < 0) return AFFQMM_E_M;
+    if (M > AFFQMM_NOALLOC_MAX_M) return AFFQMM_E_SCRATCH;
+    if (M == 0 || w->N == 0) return AFFQMM_OK;
+    if (!y) return AFFQMM_E_NULL;
+    if (!aligned(y, 2)) return AFFQMM_E_ALIGN;
+    if (w->K > 0) {
+        if (!x) return AFFQMM_E_NULL;
+        if (!aligned(x, 16)) return AFFQMM_E_ALIGN;
+    }
+    DeviceInfo* d = nullptr;
+    rc = device_info(&d);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (w->K == 0) {  // an empty sum: every output is +0
+        return cudaMemsetAsync(y, 0, (size_t)M * w->N * 2, st) == cudaSuccess ? AFFQMM_OK : AFFQMM_E_CUDA;
+    }
+    DecodePlan plan;
+    rc = plan_decode(*d, 1, w, M, &plan);
+    if (rc) return rc;
+    if (plan.ws_bytes > sizeof(g_noalloc_scratch)) return AFFQMM_E_SCRATCH;
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    // The status word and this call's merge counters (four per 128-row tile)
+    // must start at zero; whatever an earlier call left in them is cleared on
+    // the stream, ahead of the kernel.  The partial-sum slots need no clearing.
+    const size_t zeroed = kStatusBytes + (size_t)4 * (size_t)plan.p.proj[0].tiles * sizeof(uint32_t);
+    if (cudaMemsetAsync(scratch, 0, zeroed, st) != cudaSuccess) return AFFQMM_E_CUDA;
+    bind_workspace(&plan, scratch);
+    plan.p.proj[0].y = y;
+    CUtensorMap map;
+    rc = make_x_map(x, M, w->K, 16, &map);
+    if (rc) return rc;
+    if (launch_decode(w->bits, w->group, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
+    return AFFQMM_OK;
+}

@@ -26,7 +26,9 @@
  *     `stream` (a cudaStream_t; NULL means the legacy default stream) and is
  *     asynchronous: the call returns once the launches are queued.
  *   - The caller allocates and owns every buffer; the library never
- *     allocates device memory and keeps no state between calls.
+ *     allocates device memory and keeps no state between calls.  The one
+ *     exception is affqmm_run_noalloc, which works in a fixed scratch array
+ *     that the library's module places in device memory (see there).
  *   - Every argument is validated on the host before anything is launched.
  *     A rejected call returns a nonzero affqmm_status and launches nothing.
  *     Nothing is thrown or aborted across the ABI.
@@ -60,7 +62,8 @@ typedef enum {
     AFFQMM_E_TIMEOUT = 8,   /* a bounded device wait gave up (see affqmm_workspace_status) */
     AFFQMM_E_CUDA = 9,      /* a CUDA runtime call or launch failed */
     AFFQMM_E_ARG = 10,      /* other bad argument: count, mismatched stacked weights */
-    AFFQMM_E_DEVICE = 11    /* the current device is not an sm_103 GPU */
+    AFFQMM_E_DEVICE = 11,   /* the current device is not an sm_103 GPU */
+    AFFQMM_E_SCRATCH = 12   /* affqmm_run_noalloc: the call needs more than its built-in scratch */
 } affqmm_status;
 
 /* Largest M one call accepts (larger batches: split them). */
@@ -152,6 +155,44 @@ AFFQMM_API int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* str
  * `stream`).  Returns AFFQMM_OK, or AFFQMM_E_TIMEOUT when a kernel that used
  * this workspace gave up a bounded wait (its outputs are then invalid). */
 AFFQMM_API int affqmm_workspace_status(void* workspace, void* stream);
+
+/* Largest M affqmm_run_noalloc takes, and the size of its built-in scratch. */
+#define AFFQMM_NOALLOC_MAX_M 16
+#define AFFQMM_NOALLOC_SCRATCH_BYTES (3u << 20)
+
+/* affqmm_run for M <= 16 activation rows without any device memory from the
+ * caller beyond x and y.  The paper has no counterpart to this entry point:
+ * it is a convenience of this library.
+ *
+ * Who needs it: code that runs where it cannot allocate device memory -- a
+ * plug-in inside a host engine that owns all of the GPU's memory and hands
+ * its plug-ins no allocator, or a latency-critical loop that must not call
+ * cudaMalloc/cudaFree (they can synchronize the device) once it has started.
+ * Such callers cannot supply the workspace affqmm_run wants, so this call
+ * uses a scratch array of AFFQMM_NOALLOC_SCRATCH_BYTES (3 MiB) that the
+ * library itself places in device memory; every GPU that loads the library
+ * holds it until the process exits.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ *   w, x, y, stream  as affqmm_run (x 16-byte aligned, y fully written)
+ *
+ * - The first call on a device finds the scratch's device address (once per
+ *   device, with that device current) and sets the kernels' shared-memory
+ *   limits; make that first call before any stream capture.
+ * - Every call on a device shares the one scratch array, which keeps what the
+ *   last call left there.  The call clears the parts that must start at zero
+ *   (a status word and the merge counters it uses) on `stream` before its
+ *   kernel runs.  Calls that overlap on the GPU (different streams, different
+ *   host threads without ordering) race on the scratch and give wrong
+ *   results: order them on one stream.
+ * - This call cannot report a bounded device wait that gave up (never
+ *   expected on a healthy GPU; y is then unspecified).  Callers that need
+ *   that report use affqmm_run and affqmm_workspace_status.
+ * Same result, bit for bit, as affqmm_run on the same inputs.
+ * Errors: as affqmm_run (no E_WORKSPACE), plus E_SCRATCH when M > 16 or when
+ * the split of the work on this device would need more than the scratch. */
+AFFQMM_API int affqmm_run_noalloc(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

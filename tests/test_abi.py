@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_strerror_names_every_status(L):
     seen = set()
-    for code in range(12):
+    for code in range(13):
         s = api.strerror(code)
         assert s and s not in seen
         seen.add(s)
