@@ -89,7 +89,6 @@ cudaError_t decode_allow_smem();
 cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st);
 constexpr int kDecodeSmemMax = 200 * 1024;
 // prompt.cu: the tensor map describes x [M, K] bf16 with a 64 x 128 box.
-size_t prompt_smem_bytes();
 cudaError_t prompt_allow_smem();
 cudaError_t launch_prompt(int bits, const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st);
 cudaError_t launch_pack(int bits, int group, int64_t N, int64_t K, const uint8_t* codes,

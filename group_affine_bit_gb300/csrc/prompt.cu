@@ -1,35 +1,39 @@
-// prompt.cu -- the compute-bound projection for prompt chunks of up to 128
+// prompt.cu -- the compute-bound projection for prompt chunks of 17..128
 // activation rows, on the 5th-generation tensor cores (tcgen05, TMEM).
 //
-// One CTA per SM.  Its work is a contiguous run of (256-row tile, 128-deep
-// block) units ("stream-K"), cut so every SM gets the same number of units.
-// Per unit:
-//   * a TMA warp loads the 128 x 128 activation tile (two 64-wide panels,
-//     128-byte swizzle, rows past M and depth past K filled with zeros);
-//   * eight dequantization warps, one thread per weight row, read the row's
-//     codes of the unit's two packed 128-row blocks from HBM (one unit
-//     ahead, in registers), round every weight once as
-//     bf16(fma(s, q, b)) -- the same device arithmetic as the decode kernel
-//     -- and write them into shared memory in the tensor core's K-major,
-//     128-byte-swizzled layout (prior art: the affine_mm prompt GEMM of the
-//     "Gemma 4 12B on the native Metal engine" page, which dequantizes into
-//     the threadgroup tile and lets the tensor unit accumulate over the whole
-//     depth);
-//   * one thread issues tcgen05.mma (kind::f16, M = 128 activation rows,
-//     N = 256 weight rows, K = 16) accumulating in fp32 in TMEM, and commits
-//     to the stage's "empty" barrier;
-//   * at the end of a tile's segment four epilogue warps read TMEM with
-//     tcgen05.ld and either store bf16 y (the whole tile was this CTA's) or
-//     an fp32 partial that the last CTA to finish the tile adds up in k order
-//     (an atomic counter per tile and 32-row quarter, no waiting).
-// Two shared-memory stages of 96 KB (32 KB activations + 64 KB weights).
+// The weights are the A operand and live in tensor memory; the activations
+// are the B operand in shared memory.  One CTA per SM works on a contiguous
+// run of units ("stream-K"); a unit is a 256-row tile pair (two 128-row
+// layout tiles) x one 128-deep block.  Per unit:
+//   * a producer thread copies the unit's 128 x 128 activation tile (TMA,
+//     two 64-wide panels, 128-byte swizzle, rows past M and depth past K read
+//     as zero) and the two packed weight blocks (one bulk copy each, about
+//     9 KB at 4 bits) into one shared-memory stage of a ring;
+//   * two dequantization groups of four warps -- one per 128-row layout
+//     tile, one thread per weight row -- read their row's codes back, round
+//     every weight once as bf16(fma(s, q, b)) (affqmm_format.cuh, the same
+//     device arithmetic as the decode kernel) and store the row into a
+//     tensor-memory A buffer with tcgen05.st.  Units alternate between two
+//     such pairs of groups, each with its own A buffers, so one unit is
+//     dequantized while the MMAs of the previous one run;
+//   * one thread issues the unit's MMAs (M = 128 weight rows, N = activation
+//     rows rounded up to 16, K = 16): two chains, one per layout tile, each
+//     accumulating over the tile's whole depth in fp32 in tensor memory;
+//   * at the end of a tile's segment four epilogue warps read the two
+//     accumulators with tcgen05.ld and store bf16 y, or, when several runs
+//     share the tile, an fp32 partial; a second, small kernel then adds each
+//     shared tile's partials in run (k) order, every output in parallel.
+// Prior art: the affine_mm prompt GEMM of the "Gemma 4 12B on the native
+// Metal engine" page, which dequantizes each weight as bf16(fma(scale, code,
+// bias)) into the tile and lets the tensor unit accumulate over the whole
+// depth; on GB300 the dequantized tile goes to tensor memory, which keeps
+// the shared-memory traffic to the activations and the packed codes.
 // Every mbarrier wait is bounded; a wait that gives up sets the workspace
 // status word and a CTA-wide abort flag, and every role then finishes.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <cstddef>
-#include <type_traits>
 
 #include "affqmm_async.cuh"
 #include "affqmm_format.cuh"
@@ -39,66 +43,61 @@
 namespace affqmm {
 namespace {
 
-constexpr int P_THREADS = 14 * 32;   // TMA, MMA, 8 dequant, 4 epilogue warps
-constexpr int P_DEQ_WARP0 = 2;
-constexpr int P_EPI_WARP0 = 10;
-constexpr int P_TILE_N = 256;        // weight rows per tile (MMA N)
-constexpr int P_TILE_M = 128;        // activation rows (MMA M)
-constexpr int P_STAGES = 2;
-constexpr uint32_t P_A_BYTES = P_TILE_M * KBLK * 2;   // 32 KB
-constexpr uint32_t P_B_BYTES = P_TILE_N * KBLK * 2;   // 64 KB
-constexpr uint32_t P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr uint32_t P_A_PANEL = P_TILE_M * 128;         // one 64-deep panel
-constexpr uint32_t P_B_PANEL = P_TILE_N * 128;
-constexpr uint32_t P_TMEM_COLS = 256;
-
-constexpr uint32_t P_IDESC = idesc_bf16_f32(P_TILE_M, P_TILE_N);
-
-__device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
-
-// The 16 chunks (8 weights each) of one dequantized row into the 128-byte-
-// swizzled K-major layout: chunk c holds k = 8c .. 8c + 7, lives in panel
-// c / 8 at 16-byte position (c mod 8) xor (row mod 8) of the row's 128 bytes.
-template <int BITS, int GROUP, int C>
-__device__ __forceinline__ void store_chunks(const uint32_t* cw, const uint32_t* sbw, uint32_t rowbase, int r8) {
-    if constexpr (C < KBLK / 8) {
-        uint32_t w[4];
-        weight_pairs<BITS, GROUP, 4 * C, 4>(cw, sbw, w);
-        sts_v4(rowbase + (uint32_t)(C >> 3) * P_B_PANEL + ((uint32_t)((C & 7) ^ r8) << 4), w[0], w[1], w[2], w[3]);
-        store_chunks<BITS, GROUP, C + 1>(cw, sbw, rowbase, r8);
-    }
-}
+constexpr int P_DEQ_GROUPS = 4;                                  // (layout tile, unit parity)
+constexpr int P_DEQ_WARP0 = 2;                                   // warp 0: producer, 1: MMA
+constexpr int P_EPI_WARP0 = P_DEQ_WARP0 + 4 * P_DEQ_GROUPS;      // 18
+constexpr int P_THREADS = (P_EPI_WARP0 + 4) * 32;                // 704
+constexpr int P_TILE_N = 256;                                    // weight rows per unit
+constexpr int P_ROWS = 128;                                      // activation rows per launch (max)
+constexpr uint32_t P_X_PANEL = P_ROWS * 128;                     // 128 rows x 64 k bf16, 16 KB
+constexpr uint32_t P_X_BYTES = 2 * P_X_PANEL;                    // one 128-deep block of x
+constexpr uint32_t P_TMEM_COLS = 512;
+constexpr uint32_t P_ACC_COLS = 128;                             // fp32 accumulator per layout tile
+constexpr uint32_t P_A_COL0 = 2 * P_ACC_COLS;                    // A buffers after the two accumulators
+constexpr uint32_t P_A_COLS = KBLK / 2;                          // 128 bf16 per row
+constexpr int P_RING_MAX = 8;
 
 struct PromptSmem {
-    uint64_t full_a[P_STAGES];
-    uint64_t full_b[P_STAGES];
-    uint64_t empty[P_STAGES];
+    uint64_t full[P_RING_MAX];
+    uint64_t empty[P_RING_MAX];
+    uint64_t a_full[P_DEQ_GROUPS];
+    uint64_t a_empty[P_DEQ_GROUPS];
     uint64_t acc_full;
     uint64_t acc_empty;
     uint32_t tmem_base;
     int abort_flag;
 };
 
+// A stage: the activation block (1024-byte aligned for the swizzle), then the
+// unit's two packed weight blocks.
+template <int BITS, int GROUP>
+constexpr uint32_t prm_stage_bytes() {
+    return (P_X_BYTES + 2u * (uint32_t)block_bytes(BITS, GROUP) + 1023u) / 1024u * 1024u;
+}
+// As many stages as fit in ~200 KB, an even number (stage s always serves
+// units of parity s mod 2, so every barrier has one set of waiters).
+constexpr int prm_ring_for(uint32_t stage) {
+    return (int)(200u * 1024u / stage) / 2 * 2 > P_RING_MAX ? P_RING_MAX : (int)(200u * 1024u / stage) / 2 * 2;
+}
+template <int BITS, int GROUP>
+constexpr int prm_ring() {
+    return prm_ring_for(prm_stage_bytes<BITS, GROUP>());
+}
+
 template <int BITS, int GROUP>
 __global__ void __launch_bounds__(P_THREADS, 1)
     prompt_kernel(const __grid_constant__ PromptParams p, const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte alignment for the swizzled panels
+    constexpr int BB = block_bytes(BITS, GROUP);
+    constexpr uint32_t STAGE = prm_stage_bytes<BITS, GROUP>();
+    constexpr int NS = prm_ring<BITS, GROUP>();
+    static_assert(NS >= 2 && NS % 2 == 0, "ring depth");
+    static_assert(BB % 16 == 0, "bulk copies move multiples of 16 bytes");
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* base_ptr = smem_raw + (base - raw);
-    PromptSmem* sh = reinterpret_cast<PromptSmem*>(base_ptr + P_STAGES * P_STAGE_BYTES);
-    const uint32_t sh_addr = base + P_STAGES * P_STAGE_BYTES;
-    auto bar_full_a = [&](int s) { return sh_addr + (uint32_t)offsetof(PromptSmem, full_a) + 8u * s; };
-    auto bar_full_b = [&](int s) { return sh_addr + (uint32_t)offsetof(PromptSmem, full_b) + 8u * s; };
-    auto bar_empty = [&](int s) { return sh_addr + (uint32_t)offsetof(PromptSmem, empty) + 8u * s; };
-    const uint32_t bar_acc_full = sh_addr + (uint32_t)offsetof(PromptSmem, acc_full);
-    const uint32_t bar_acc_empty = sh_addr + (uint32_t)offsetof(PromptSmem, acc_empty);
-    auto stage_a = [&](int s) { return base + (uint32_t)s * P_STAGE_BYTES; };
-    auto stage_b = [&](int s) { return base + (uint32_t)s * P_STAGE_BYTES + P_A_BYTES; };
-
+    PromptSmem* sh = reinterpret_cast<PromptSmem*>(smem_raw + (base - raw) + (size_t)NS * STAGE);
+    const uint32_t sh_addr = base + (uint32_t)NS * STAGE;
+#define BAR(field, i) (sh_addr + (uint32_t)offsetof(PromptSmem, field) + 8u * (uint32_t)(i))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     int pi = 0;
@@ -111,18 +110,20 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const int u1 = (int)((int64_t)(c + 1) * U / PC);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < P_STAGES; ++s) {
-            mbar_init(bar_full_a(s), 1);
-            mbar_init(bar_full_b(s), 8);  // one arrival per dequantization warp
-            mbar_init(bar_empty(s), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(BAR(full, s), 1);
+            mbar_init(BAR(empty, s), 9);  // the 8 warps that read the packed blocks, and the MMAs that read x
         }
-        mbar_init(bar_acc_full, 1);
-        mbar_init(bar_acc_empty, 4);      // one arrival per epilogue warp
+        for (int g = 0; g < P_DEQ_GROUPS; ++g) {
+            mbar_init(BAR(a_full, g), 4);
+            mbar_init(BAR(a_empty, g), 1);
+        }
+        mbar_init(BAR(acc_full, 0), 1);
+        mbar_init(BAR(acc_empty, 0), 4);  // one arrival per epilogue warp
         sh->abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1)  // TMEM for the fp32 accumulator: 128 lanes x 256 columns
-        tmem_alloc(sh_addr + (uint32_t)offsetof(PromptSmem, tmem_base), P_TMEM_COLS);
+    if (warp == 1) tmem_alloc(sh_addr + (uint32_t)offsetof(PromptSmem, tmem_base), P_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -130,188 +131,170 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     volatile int* abort_flag = &sh->abort_flag;
 
     if (warp == 0) {
-        // ---------------------------------------------------------- TMA producer
+        // ---------------------------------------------------------- producer
         if (lane == 0) {
             prefetch_tmap(&xmap);
+            const uint64_t policy = policy_evict_first();  // the weights are read once
             for (int u = u0, i = 0; u < u1; ++u, ++i) {
-                const int s = i % P_STAGES;
-                const uint32_t ph = (uint32_t)((i / P_STAGES) & 1);
-                if (!wait_or_abort(bar_empty(s), ph ^ 1u, abort_flag, p.status)) break;
-                const int kb = u % KB;
-                mbar_arrive_expect_tx(bar_full_a(s), P_A_BYTES);
-                tma_load_2d(stage_a(s), &xmap, kb * KBLK, 0, bar_full_a(s));
-                tma_load_2d(stage_a(s) + P_A_PANEL, &xmap, kb * KBLK + 64, 0, bar_full_a(s));
+                const int s = i % NS;
+                const uint32_t ph = (uint32_t)((i / NS) & 1);
+                if (!wait_or_abort(BAR(empty, s), ph ^ 1u, abort_flag, p.status)) break;
+                const int tile = u / KB, kb = u - (u / KB) * KB;
+                const int lt0 = 2 * tile;
+                const bool two = lt0 + 1 < P.ltiles;
+                const uint32_t st = base + (uint32_t)s * STAGE;
+                mbar_arrive_expect_tx(BAR(full, s), P_X_BYTES + (two ? 2u : 1u) * (uint32_t)BB);
+                tma_load_2d(st, &xmap, kb * KBLK, 0, BAR(full, s));
+                tma_load_2d(st + P_X_PANEL, &xmap, kb * KBLK + 64, 0, BAR(full, s));
+                bulk_g2s_hint(st + P_X_BYTES, P.packed + ((size_t)lt0 * KB + kb) * BB, (uint32_t)BB, BAR(full, s),
+                              policy);
+                if (two)
+                    bulk_g2s_hint(st + P_X_BYTES + (uint32_t)BB, P.packed + ((size_t)(lt0 + 1) * KB + kb) * BB,
+                                  (uint32_t)BB, BAR(full, s), policy);
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            const int nn = p.M <= 16 ? 16 : (p.M + 15) / 16 * 16;  // MMA N: activation rows
+            const uint32_t idesc = idesc_bf16_f32(128, nn);
             int seg = 0;
-            bool seg_open = false;
+            bool open = false, first = false;
+            int kb = u0 % KB;
             for (int u = u0, i = 0; u < u1; ++u, ++i) {
-                const int s = i % P_STAGES;
-                const uint32_t ph = (uint32_t)((i / P_STAGES) & 1);
-                const int kb = u % KB;
-                const bool first = !seg_open;
-                if (first) {  // the accumulator must have been drained
-                    if (!wait_or_abort(bar_acc_empty, (uint32_t)(seg & 1) ^ 1u, abort_flag, p.status)) break;
+                if (!open) {  // both accumulators must have been drained
+                    if (!wait_or_abort(BAR(acc_empty, 0), (uint32_t)(seg & 1) ^ 1u, abort_flag, p.status)) break;
                     tc_fence_after();
-                    seg_open = true;
+                    open = first = true;
                 }
-                if (!wait_or_abort(bar_full_a(s), ph, abort_flag, p.status)) break;
-                if (!wait_or_abort(bar_full_b(s), ph, abort_flag, p.status)) break;
+                const int s = i % NS;
+                const uint32_t ph = (uint32_t)((i / NS) & 1);
+                const int par = i & 1;
+                const uint32_t aph = (uint32_t)((i >> 1) & 1);
+                if (!wait_or_abort(BAR(full, s), ph, abort_flag, p.status)) break;
+                if (!wait_or_abort(BAR(a_full, par), aph, abort_flag, p.status)) break;
+                if (!wait_or_abort(BAR(a_full, 2 + par), aph, abort_flag, p.status)) break;
                 tc_fence_after();
+                const uint64_t bd0 = sw128_desc(base + (uint32_t)s * STAGE);
 #pragma unroll
-                for (int pnl = 0; pnl < 2; ++pnl) {
+                for (int k = 0; k < KBLK / 16; ++k) {
+                    // +32 bytes per 16-deep step, +16 KB per 64-deep panel (descriptor units of 16 bytes)
+                    const uint64_t bd = bd0 + (uint64_t)((k >> 2) * (P_X_PANEL >> 4) + (k & 3) * 2);
+                    const uint32_t acc = (first && k == 0) ? 0u : 1u;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sw128_desc(stage_a(s) + pnl * P_A_PANEL + kk * 32);
-                        const uint64_t bd = sw128_desc(stage_b(s) + pnl * P_B_PANEL + kk * 32);
-                        umma_ss(tmem, ad, bd, P_IDESC, (first && pnl == 0 && kk == 0) ? 0u : 1u);
-                    }
+                    for (int sub = 0; sub < 2; ++sub)
+                        umma_ts(tmem + (uint32_t)sub * P_ACC_COLS,
+                                tmem + P_A_COL0 + (uint32_t)(2 * sub + par) * P_A_COLS + 8u * k, bd, idesc, acc);
                 }
-                umma_commit(bar_empty(s));
+                first = false;
+                umma_commit(BAR(a_empty, par));
+                umma_commit(BAR(a_empty, 2 + par));
+                umma_commit(BAR(empty, s));
                 if (kb == KB - 1 || u == u1 - 1) {
-                    umma_commit(bar_acc_full);
+                    umma_commit(BAR(acc_full, 0));
                     ++seg;
-                    seg_open = false;
+                    open = false;
                 }
+                if (++kb == KB) kb = 0;
             }
         }
     } else if (warp < P_EPI_WARP0) {
         // ---------------------------------------------------------- dequantization
-        // thread = weight row n of the 256-row tile (two 128-row layout tiles)
-        const int n = 32 * (warp - P_DEQ_WARP0) + lane;
-        const int sub = n >> 7, nn = n & 127;
-        constexpr int BB = block_bytes(BITS, GROUP);
-        uint32_t cw[2][4 * BITS];
-        uint32_t sbw[2][sb_words(GROUP)];
-        auto load_unit = [&](int u, auto bufc) {
-            constexpr int buf = decltype(bufc)::value;
-            const int tile = u / KB, kb = u % KB;
-            const int lt = 2 * tile + sub;  // layout tile of this row
-            if (lt < P.ltiles) {
-                const uint8_t* blk = P.packed + ((size_t)lt * KB + kb) * BB;
-                load_row_codes<BITS>(blk, nn, cw[buf]);
-                load_row_sb<GROUP>(blk + sb_offset(BITS, GROUP, nn), sbw[buf]);
-            } else {  // rows past the last tile: zero weights
+        // group g: layout tile `sub` of the units of parity `par`; thread =
+        // weight row 32q + lane of that layout tile (TMEM lane quarter q)
+        const int g = (warp - P_DEQ_WARP0) >> 2;
+        const int sub = g >> 1, par = g & 1;
+        const int abuf = 2 * sub + par;
+        const int q = warp & 3;
+        const int n_in = 32 * q + lane;
+        for (int u = u0 + par, i = par; u < u1; u += 2, i += 2) {
+            const int s = i % NS;
+            const uint32_t ph = (uint32_t)((i / NS) & 1);
+            const uint32_t aph = (uint32_t)((i >> 1) & 1);
+            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), ph, abort_flag, p.status))) break;
+            const int tile = u / KB;
+            const bool present = 2 * tile + sub < P.ltiles;
+            uint32_t cw[4 * BITS];
+            uint32_t sbw[sb_words(GROUP)];
+            if (present) {
+                const uint32_t blk = base + (uint32_t)s * STAGE + P_X_BYTES + (uint32_t)(sub * BB);
+                load_row_codes_smem<BITS>(blk, n_in, cw);
+                load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, n_in), sbw);
+            } else {  // rows past the last layout tile: zero weights
 #pragma unroll
-                for (int w = 0; w < 4 * BITS; ++w) cw[buf][w] = 0u;
+                for (int w = 0; w < 4 * BITS; ++w) cw[w] = 0u;
 #pragma unroll
-                for (int w = 0; w < sb_words(GROUP); ++w) sbw[buf][w] = 0u;
+                for (int w = 0; w < sb_words(GROUP); ++w) sbw[w] = 0u;
             }
-        };
-        auto store_unit = [&](int s, auto bufc) {
-            constexpr int buf = decltype(bufc)::value;
-            const uint32_t rowbase = stage_b(s) + (uint32_t)(n >> 3) * 1024u + (uint32_t)(n & 7) * 128u;
-            store_chunks<BITS, GROUP, 0>(cw[buf], sbw[buf], rowbase, n & 7);
-        };
-        using B0 = std::integral_constant<int, 0>;
-        using B1 = std::integral_constant<int, 1>;
-        if (u0 < u1) load_unit(u0, B0{});
-        for (int u = u0, i = 0; u < u1; ++u, ++i) {
-            const int s = i % P_STAGES;
-            const uint32_t ph = (uint32_t)((i / P_STAGES) & 1);
-            const bool even = (i & 1) == 0;
-            if (u + 1 < u1) {  // next unit's codes in flight while this one is dequantized
-                if (even) load_unit(u + 1, B1{});
-                else load_unit(u + 1, B0{});
-            }
-            if (!__all_sync(0xffffffffu, wait_or_abort(bar_empty(s), ph ^ 1u, abort_flag, p.status))) break;
-            if (even) store_unit(s, B0{});
-            else store_unit(s, B1{});
-            fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_full_b(s));
+            if (lane == 0) mbar_arrive(BAR(empty, s));  // codes are in registers
+            uint32_t w[32];
+            weight_pairs<BITS, GROUP, 0, 32>(cw, sbw, w);
+            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, abuf), aph ^ 1u, abort_flag, p.status))) break;
+            tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + P_A_COL0 + (uint32_t)abuf * P_A_COLS;
+            tmem_st32(ta, w);
+            tmem_st_wait();
+            weight_pairs<BITS, GROUP, 32, 32>(cw, sbw, w);
+            tmem_st32(ta + 32, w);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(a_full, abuf));
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-        const int m = 32 * quarter + lane;       // activation row of this thread
+        const int q = warp & 3;               // TMEM lanes 32q .. 32q + 31: weight rows
+        const int n_in = 32 * q + lane;
         const int M = p.M;
+        const int nchunks = (M + 31) / 32;    // 32-column pieces of the accumulators to read
         int seg = 0;
         int seg_start = u0;
         for (int u = u0; u < u1; ++u) {
-            const int kb = u % KB;
-            if (!(kb == KB - 1 || u == u1 - 1)) continue;
             const int tile = u / KB;
+            const int kb = u - tile * KB;
+            if (!(kb == KB - 1 || u == u1 - 1)) continue;
             const bool whole = (seg_start == tile * KB) && (kb == KB - 1);
-            if (!__all_sync(0xffffffffu, wait_or_abort(bar_acc_full, (uint32_t)(seg & 1), abort_flag, p.status))) break;
+            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(acc_full, 0), (uint32_t)(seg & 1), abort_flag, p.status)))
+                break;
             tc_fence_after();
-            const int64_t n_base = (int64_t)tile * P_TILE_N;
             const int slot = P.slot_begin + 2 * c + (seg_start == u0 ? 0 : 1);
-            float* srow = p.slots + (size_t)slot * (P_TILE_M * P_TILE_N) + (size_t)m * P_TILE_N;
+            float* sp = p.slots + (size_t)slot * kPromptSlotFloats;
 #pragma unroll 1
-            for (int cc = 0; cc < P_TILE_N / 32; ++cc) {
-                uint32_t vr[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(32 * cc), vr);
-                float v[32];
+            for (int sub = 0; sub < 2; ++sub) {
+                const int64_t n = (int64_t)tile * P_TILE_N + sub * 128 + n_in;
+#pragma unroll 1
+                for (int cc = 0; cc < nchunks; ++cc) {
+                    uint32_t vr[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)sub * P_ACC_COLS + 32u * cc, vr);
+                    const int mb = 32 * cc;
+                    if (whole) {
+                        if (n < P.N) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(vr[e]);
-                if (whole) {
-                    if (m < M) {
-                        for (int e = 0; e < 32; ++e) {
-                            const int64_t n = n_base + 32 * cc + e;
-                            if (n < P.N) P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v[e]));
+                            for (int e = 0; e < 32; ++e)
+                                if (mb + e < M)
+                                    P.y[(int64_t)(mb + e) * P.N + n] =
+                                        __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(vr[e])));
                         }
-                    }
-                } else {
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        __stcg(reinterpret_cast<float4*>(srow + 32 * cc + e), make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
+                        for (int e = 0; e < 32; ++e)
+                            if (mb + e < M) __stcg(sp + (size_t)(mb + e) * P_TILE_N + sub * 128 + n_in, __uint_as_float(vr[e]));
+                    }
                 }
             }
-            // accumulator drained: the MMA warp may start the next segment
+            // accumulators drained: the MMA thread may start the next segment
+            // (a partial is added to the other runs' by prompt_merge_kernel)
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acc_empty);
-            if (!whole) {
-                // Publish this warp's 32 rows of the partial; the last CTA to
-                // arrive (per tile and row quarter) adds them in k order.
-                __syncwarp();
-                unsigned prev = 0;
-                unsigned* ctr = &p.counters[(size_t)(P.ctr_begin + tile) * 4 + quarter];
-                if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
-                __syncwarp();
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                const int t0 = tile * KB, t1 = t0 + KB - 1;
-                const int cf = (int)(((int64_t)(t0 + 1) * PC - 1) / U);
-                const int cl = (int)(((int64_t)(t1 + 1) * PC - 1) / U);
-                if (prev == (unsigned)(cl - cf)) {
-#pragma unroll 1
-                    for (int cc = 0; cc < P_TILE_N / 32; ++cc) {
-                        float acc[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-                        for (int cb = cf; cb <= cl; ++cb) {
-                            const int bcb = (int)((int64_t)cb * U / PC);
-                            const int sc = P.slot_begin + 2 * cb + (bcb >= t0 ? 0 : 1);
-                            const float* row = p.slots + (size_t)sc * (P_TILE_M * P_TILE_N) + (size_t)m * P_TILE_N + 32 * cc;
-#pragma unroll
-                            for (int e = 0; e < 32; e += 4) {
-                                const float4 f = __ldcg(reinterpret_cast<const float4*>(row + e));
-                                acc[e] += f.x;
-                                acc[e + 1] += f.y;
-                                acc[e + 2] += f.z;
-                                acc[e + 3] += f.w;
-                            }
-                        }
-                        if (m < M) {
-                            for (int e = 0; e < 32; ++e) {
-                                const int64_t n = n_base + 32 * cc + e;
-                                if (n < P.N) P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
-                            }
-                        }
-                    }
-                    if (lane == 0) *ctr = 0u;
-                }
-            }
+            if (lane == 0) mbar_arrive(BAR(acc_empty, 0));
             ++seg;
             seg_start = u + 1;
         }
     }
+#undef BAR
 
-    // teardown: every role has left its loop
+    // teardown: every role has left its loop and nothing is in flight
     __syncwarp();
     tc_fence_before();
     __syncthreads();
@@ -321,9 +304,54 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
 }
 
+// The tiles that several runs share: y = the runs' fp32 partials added in run
+// order.  Grid: (every tile of every projection, 16-row blocks of the
+// activation rows); thread = one of the tile's 256 weight rows.  Tiles that
+// one run owned were stored by prompt_kernel and are skipped.
+__global__ void __launch_bounds__(P_TILE_N) prompt_merge_kernel(const __grid_constant__ PromptParams p) {
+    const int t_all = (int)blockIdx.x;
+    int pi = 0;
+    for (int i = 1; i < p.nproj; ++i)
+        if (t_all >= p.proj[i].ctr_begin) pi = i;
+    const PromptProj& P = p.proj[pi];
+    const int tile = t_all - P.ctr_begin;
+    const int U = P.units, PC = P.nctas, KB = p.KB;
+    const int t0 = tile * KB, t1 = t0 + KB - 1;
+    const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
+    if (cf == cl) return;
+    const int nt = (int)threadIdx.x;
+    const int64_t n = (int64_t)tile * P_TILE_N + nt;
+    const int m0 = 16 * (int)blockIdx.y;
+    if (n >= P.N || m0 >= p.M) return;
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int cb = cf; cb <= cl; ++cb) {
+        const int b0 = (int)((int64_t)cb * U / PC);
+        const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
+        const float* src = p.slots + (size_t)sc * kPromptSlotFloats + (size_t)m0 * P_TILE_N + nt;
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            if (m0 + e < p.M) acc[e] += __ldcg(src + (size_t)e * P_TILE_N);
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        if (m0 + e < p.M) P.y[(int64_t)(m0 + e) * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
+}
+
+template <int BITS, int GROUP>
+size_t prompt_smem_for() {
+    return (size_t)prm_ring<BITS, GROUP>() * prm_stage_bytes<BITS, GROUP>() + sizeof(PromptSmem) + 1024;
+}
+
 template <int BITS, int GROUP>
 cudaError_t launch_prompt_bg(const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    prompt_kernel<BITS, GROUP><<<grid, P_THREADS, prompt_smem_bytes(), st>>>(p, map);
+    prompt_kernel<BITS, GROUP><<<grid, P_THREADS, prompt_smem_for<BITS, GROUP>(), st>>>(p, map);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const PromptProj& last = p.proj[p.nproj - 1];
+    const dim3 mgrid((unsigned)(last.ctr_begin + last.tiles), (unsigned)((p.M + 15) / 16));
+    prompt_merge_kernel<<<mgrid, P_TILE_N, 0, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -334,21 +362,20 @@ cudaError_t launch_prompt_b(const PromptParams& p, const CUtensorMap& map, int g
     return launch_prompt_bg<BITS, 128>(p, map, grid, st);
 }
 
+template <int BITS, int GROUP>
+cudaError_t allow_prompt_bg() {
+    return cudaFuncSetAttribute(prompt_kernel<BITS, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)prompt_smem_for<BITS, GROUP>());
+}
+
 template <int BITS>
 cudaError_t allow_prompt_b() {
-    for (cudaError_t e : {cudaFuncSetAttribute(prompt_kernel<BITS, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)prompt_smem_bytes()),
-                          cudaFuncSetAttribute(prompt_kernel<BITS, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)prompt_smem_bytes()),
-                          cudaFuncSetAttribute(prompt_kernel<BITS, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)prompt_smem_bytes())})
+    for (cudaError_t e : {allow_prompt_bg<BITS, 32>(), allow_prompt_bg<BITS, 64>(), allow_prompt_bg<BITS, 128>()})
         if (e != cudaSuccess) return e;
     return cudaSuccess;
 }
 
 }  // namespace
-
-size_t prompt_smem_bytes() { return (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PromptSmem) + 1024; }
 
 cudaError_t prompt_allow_smem() {
     for (cudaError_t e : {allow_prompt_b<2>(), allow_prompt_b<3>(), allow_prompt_b<4>(), allow_prompt_b<5>(),
