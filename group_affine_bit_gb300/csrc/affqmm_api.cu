@@ -148,7 +148,8 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// x [M, K] bf16 row-major as 64 (k) x `box_rows` boxes with the 128-byte
+// x [M, K] bf16 row-major as 64 (k) x `box_rows` boxes (the decode kernel
+// loads M rows, the prompt kernel 128) with the 128-byte
 // swizzle the tensor core reads; rows past M and k past K read as zero.
 int make_x_map(const uint16_t* x, int64_t M, int64_t K, int box_rows, CUtensorMap* map) {
     EncodeTiledFn fn = encode_tiled();
@@ -278,7 +279,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         bind_workspace(&plan, workspace);
         for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i];
         CUtensorMap map;
-        rc = make_x_map(x, M, K, 16, &map);
+        rc = make_x_map(x, M, K, (int)M, &map);
         if (rc) return rc;
         if (launch_decode(ws[0].bits, ws[0].group, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
         return AFFQMM_OK;
@@ -482,7 +483,7 @@ extern "C" int affqmm_run_noalloc(const affqmm_weight* w, const uint16_t* x, int
     bind_workspace(&plan, scratch);
     plan.p.proj[0].y = y;
     CUtensorMap map;
-    rc = make_x_map(x, M, w->K, 16, &map);
+    rc = make_x_map(x, M, w->K, (int)M, &map);
     if (rc) return rc;
     if (launch_decode(w->bits, w->group, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
     return AFFQMM_OK;

@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "affqmm.h"
 
@@ -82,12 +83,29 @@ struct PromptParams {
 
 constexpr size_t kPromptSlotFloats = 128 * 256;
 
+// Launch `kernel` with programmatic stream serialization: it may begin while
+// the previous kernel in the stream finishes, and resolves the dependency
+// itself (griddepcontrol.wait) before it touches data that kernel may use.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), int grid, int threads, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Launchers (decode.cu, prompt.cu, pack.cu).  They return the launch's error.
-// decode.cu: the tensor map describes x [M, K] bf16 with a 64 x 16 box.
-size_t decode_smem_bytes(int bits, int group);
+// decode.cu: the tensor map describes x [M, K] bf16 with a 64 x M box.
 cudaError_t decode_allow_smem();
 cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st);
-constexpr int kDecodeSmemMax = 200 * 1024;
 // prompt.cu: the tensor map describes x [M, K] bf16 with a 64 x 128 box.
 cudaError_t prompt_allow_smem();
 cudaError_t launch_prompt(int bits, const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st);

@@ -138,6 +138,35 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return true;
 }
 
+// The same for threads that are not on the critical path (the producers,
+// which run a ring's depth ahead): between polls the thread sleeps, so its
+// polling does not take issue slots from the dequantization warps.
+__device__ __forceinline__ bool wait_or_abort_lazy(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                   uint32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            atomicOr(status, 1u);
+            return false;
+        }
+        __nanosleep(200);
+    }
+    return true;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue (and its weight copies) on SMs this grid has left, and wait for
+// the previous kernel's results (and memory) before touching global data
+// that it may have written or may still read.  Both are no-ops without the
+// launch attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // The CTA whose run holds unit u when U units are cut into PC runs
 // (run c = [floor(c*U/PC), floor((c+1)*U/PC))).
 __device__ __forceinline__ int run_of(int u, int U, int PC) { return (int)(((int64_t)(u + 1) * PC - 1) / U); }

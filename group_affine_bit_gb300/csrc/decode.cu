@@ -4,10 +4,11 @@
 // Each 128-row x 128-deep weight block is one tcgen05.mma problem:
 // D[128 weight rows, 16 activation rows] += W (tensor memory) * x^T (shared
 // memory), fp32 in tensor memory.  Per CTA:
-//   * a producer warp streams blocks (9 KB for 4-bit codes and bf16
-//     scale/bias words) with one 1-D bulk copy each into a ring of shared-
-//     memory stages, together with the block's 16 x 128 activation tile (TMA,
-//     128-byte swizzle, rows past M read as zero);
+//   * two producer threads stream the blocks (9 KB for 4-bit codes and bf16
+//     scale/bias words) two at a time with 1-D bulk copies into a ring of
+//     weight slots, and a third loads each block's M x 128 activation rows
+//     (TMA, 128-byte swizzle) into a ring of 16-row tiles whose other rows
+//     stay zero;
 //   * four lanes of work take blocks i = 0, 1, 2, 3 (mod 4) of the run; each
 //     has a group of four dequantization warps -- one thread per weight row
 //     reads the row's codes back, rounds every weight once as
@@ -38,6 +39,7 @@
 #include <cuda_bf16.h>
 
 #include <cstddef>
+#include <type_traits>
 
 #include "affqmm_async.cuh"
 #include "affqmm_format.cuh"
@@ -48,9 +50,11 @@ namespace affqmm {
 namespace {
 
 constexpr int D_LANES = 4;            // (dequant group, MMA issuer, A buffer, chain) lanes of work
-constexpr int D_THREADS = (1 + D_LANES + 4 * D_LANES) * 32;  // producer, 4 issuers, 4 groups of 4 warps
-constexpr int D_ISSUER0 = 1;
-constexpr int D_DEQ_WARP0 = 1 + D_LANES;
+constexpr int D_ISSUER0 = 1;                       // warp 0: weights producer of the even blocks
+constexpr int D_DEQ_WARP0 = 1 + D_LANES;           // then 4 issuers, 4 groups of 4 dequant warps
+constexpr int D_WPROD1 = D_DEQ_WARP0 + 4 * D_LANES; // weights producer of the odd blocks
+constexpr int D_XPROD = D_WPROD1 + 1;              // activations producer
+constexpr int D_THREADS = (D_XPROD + 1) * 32;
 constexpr int D_MMA_N = 16;           // activation rows per MMA (M <= 16)
 constexpr uint32_t D_X_PANEL = D_MMA_N * 128;      // 16 rows x 64 k bf16, 2 KB
 constexpr uint32_t D_X_BYTES = 2 * D_X_PANEL;      // one 128-deep block of x
@@ -61,35 +65,40 @@ constexpr uint32_t D_ACC_COL0 = D_LANES * D_A_COLS;
 // two segments' worth so the next segment starts while the last one is
 // drained: column D_ACC_COL0 + 16 * (D_LANES * segment buffer + chain).
 constexpr uint32_t D_IDESC = idesc_bf16_f32(128, D_MMA_N);
-constexpr int D_RING_MAX = 12;
+// Two rings: activation blocks (held until the block's MMAs are done) and
+// packed weight blocks (held only until the dequantization warps have the
+// codes in registers, so the weight ring covers the HBM latency).  Both
+// depths are multiples of the lanes: slot s always belongs to lane s mod 4,
+// so no barrier is waited on by two threads that could be a phase apart.
+constexpr int D_XRING = 16;
+constexpr int D_WRING_MAX = 24;
+constexpr uint32_t kDecRingBudget = 210u * 1024u;
 
 struct DecSmem {
-    uint64_t full[D_RING_MAX];
-    uint64_t empty[D_RING_MAX];
-    uint64_t a_full[D_LANES];
-    uint64_t a_empty[D_LANES];
+    uint64_t wfull[D_WRING_MAX];
+    uint64_t wempty[D_WRING_MAX];
+    uint64_t xfull[D_XRING];
+    uint64_t xempty[D_XRING];
+    uint64_t a_full[2 * D_LANES];   // (lane, half of the block's depth)
+    uint64_t a_empty[2 * D_LANES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort_flag;
 };
 
-template <int BITS, int GROUP>
-constexpr uint32_t dec_stage_bytes() {
-    return (uint32_t)((block_bytes(BITS, GROUP) + 1023) / 1024 * 1024) + D_X_BYTES;  // codes, then x (1 KB aligned)
+__device__ __forceinline__ void sts_zero16(uint32_t a) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
 }
-// Ring depth: a stage is refilled once the MMAs of its block are done, so the
-// ring takes as many stages as fit in ~200 KB, a multiple of the work lanes
-// (stage s always belongs to lane s mod 4: no barrier is waited on by two
-// threads that could be a phase apart).
-constexpr int dec_ring_for(uint32_t stage_bytes) {
-    return (int)(200u * 1024u / stage_bytes) / D_LANES * D_LANES > D_RING_MAX
-               ? D_RING_MAX
-               : (int)(200u * 1024u / stage_bytes) / D_LANES * D_LANES;
+
+constexpr int dec_wring_for(int block) {
+    return (int)((kDecRingBudget - D_XRING * D_X_BYTES) / (uint32_t)block) / D_LANES * D_LANES > D_WRING_MAX
+               ? D_WRING_MAX
+               : (int)((kDecRingBudget - D_XRING * D_X_BYTES) / (uint32_t)block) / D_LANES * D_LANES;
 }
 template <int BITS, int GROUP>
-constexpr int dec_ring() {
-    return dec_ring_for(dec_stage_bytes<BITS, GROUP>());
+constexpr int dec_wring() {
+    return dec_wring_for(block_bytes(BITS, GROUP));
 }
 
 template <int BITS, int GROUP>
@@ -97,14 +106,17 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     decode_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int BB = block_bytes(BITS, GROUP);
-    constexpr uint32_t STAGE = dec_stage_bytes<BITS, GROUP>();
-    constexpr uint32_t X_OFF = STAGE - D_X_BYTES;
-    constexpr int NS = dec_ring<BITS, GROUP>();
-    static_assert(NS >= D_LANES && NS % D_LANES == 0, "ring depth");
+    constexpr int NW = dec_wring<BITS, GROUP>();
+    constexpr int NP = NW / 2;  // weight slots go in pairs: slot pair q serves lanes 2(q mod 2), 2(q mod 2) + 1
+    constexpr int NX = D_XRING;
+    static_assert(NW >= D_LANES && NW % D_LANES == 0 && NX % D_LANES == 0, "ring depths");
+    static_assert(BB % 16 == 0, "bulk copies move multiples of 16 bytes");
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    DecSmem* sh = reinterpret_cast<DecSmem*>(smem_raw + (base - raw) + (size_t)NS * STAGE);
-    const uint32_t sh_addr = base + (uint32_t)NS * STAGE;
+    const uint32_t base = (raw + 1023u) & ~1023u;          // activation ring (1024-aligned for the swizzle)
+    const uint32_t wbase = base + (uint32_t)NX * D_X_BYTES;  // weight ring
+    const uint32_t ring_bytes = (uint32_t)NX * D_X_BYTES + (uint32_t)NW * BB;
+    DecSmem* sh = reinterpret_cast<DecSmem*>(smem_raw + (base - raw) + ring_bytes);
+    const uint32_t sh_addr = base + ring_bytes;
 #define BAR(field, i) (sh_addr + (uint32_t)offsetof(DecSmem, field) + 8u * (uint32_t)(i))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -118,11 +130,15 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     const int u1 = (int)((int64_t)(c + 1) * U / PC);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(BAR(full, s), 1);
-            mbar_init(BAR(empty, s), 5);  // the four warps of the block's group read the codes, its MMAs read x
+        for (int s = 0; s < NP; ++s) {
+            mbar_init(BAR(wfull, s), 1);
+            mbar_init(BAR(wempty, s), 8);  // the four warps of each of the pair's two groups read the codes
         }
-        for (int l = 0; l < D_LANES; ++l) {
+        for (int s = 0; s < NX; ++s) {
+            mbar_init(BAR(xfull, s), 1);
+            mbar_init(BAR(xempty, s), 1);  // the block's MMAs read x
+        }
+        for (int l = 0; l < 2 * D_LANES; ++l) {
             mbar_init(BAR(a_full, l), 4);
             mbar_init(BAR(a_empty, l), 1);
         }
@@ -134,32 +150,55 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         fence_mbar_init();
     }
     if (warp == D_ISSUER0) tmem_alloc(sh_addr + (uint32_t)offsetof(DecSmem, tmem_base), D_TMEM_COLS);
+    // The activation tiles' rows M..15 stay zero for the whole launch: the
+    // TMA loads write rows 0..M-1 only (the tensor map's box is M rows).
+    for (uint32_t off = 16u * threadIdx.x; off < (uint32_t)NX * D_X_BYTES; off += 16u * D_THREADS)
+        sts_zero16(base + off);
+    fence_proxy_async_smem();  // generic-proxy zeros -> TMA writes and tensor-core reads
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort_flag = &sh->abort_flag;
+    if (threadIdx.x == 0) pdl_launch_dependents();
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
+    if (warp == 0 || warp == D_WPROD1) {
+        // ---------------------------------------------------------- weights producers
+        // Blocks go in pairs (two consecutive blocks are contiguous, ~18 KB:
+        // a bulk copy moves data faster the larger it is), and two threads in
+        // two warps take alternate pairs.  The weights never depend on an
+        // earlier kernel, so these threads start before the grid dependency
+        // is resolved.
+        if (lane == 0) {
+            const int pp = warp == 0 ? 0 : 1;
+            const uint64_t policy = policy_evict_first();  // the weights are read once
+            const int n = u1 - u0;
+            for (int j = pp; 2 * j < n; j += 2) {
+                const int ps = j % NP;
+                const uint32_t ph = (uint32_t)((j / NP) & 1);
+                if (!wait_or_abort_lazy(BAR(wempty, ps), ph ^ 1u, abort_flag, p.status)) break;
+                const uint32_t bytes = (2 * j + 1 < n ? 2u : 1u) * (uint32_t)BB;
+                mbar_arrive_expect_tx(BAR(wfull, ps), bytes);
+                bulk_g2s_hint(wbase + (uint32_t)ps * (2u * BB), P.packed + (size_t)(u0 + 2 * j) * BB, bytes,
+                              BAR(wfull, ps), policy);
+            }
+        }
+    } else if (warp == D_XPROD) {
+        // ---------------------------------------------------------- activations producer
         if (lane == 0) {
             prefetch_tmap(&xmap);
-            const uint64_t policy = policy_evict_first();  // the weights are read once
-            int s = 0;
-            uint32_t ph = 0;
+            pdl_wait();  // x may come from the previous kernel
+            const uint32_t x_bytes = 2u * 64u * 2u * (uint32_t)p.M;  // two panels of M rows
             int kb = u0 % KB;
-            for (int u = u0; u < u1; ++u) {
-                if (!wait_or_abort(BAR(empty, s), ph ^ 1u, abort_flag, p.status)) break;
-                const uint32_t st = base + (uint32_t)s * STAGE;
-                mbar_arrive_expect_tx(BAR(full, s), (uint32_t)BB + D_X_BYTES);
-                bulk_g2s_hint(st, P.packed + (size_t)u * BB, (uint32_t)BB, BAR(full, s), policy);
-                tma_load_2d(st + X_OFF, &xmap, kb * KBLK, 0, BAR(full, s));
-                tma_load_2d(st + X_OFF + D_X_PANEL, &xmap, kb * KBLK + 64, 0, BAR(full, s));
+            for (int u = u0, i = 0; u < u1; ++u, ++i) {
+                const int s = i % NX;
+                const uint32_t ph = (uint32_t)((i / NX) & 1);
+                if (!wait_or_abort_lazy(BAR(xempty, s), ph ^ 1u, abort_flag, p.status)) break;
+                const uint32_t st = base + (uint32_t)s * D_X_BYTES;
+                mbar_arrive_expect_tx(BAR(xfull, s), x_bytes);
+                tma_load_2d(st, &xmap, kb * KBLK, 0, BAR(xfull, s));
+                tma_load_2d(st + D_X_PANEL, &xmap, kb * KBLK + 64, 0, BAR(xfull, s));
                 if (++kb == KB) kb = 0;
-                if (++s == NS) {
-                    s = 0;
-                    ph ^= 1u;
-                }
             }
         }
     } else if (warp < D_DEQ_WARP0) {
@@ -183,24 +222,32 @@ __global__ void __launch_bounds__(D_THREADS, 1)
                     open = true;
                 }
                 if ((i & (D_LANES - 1)) == e) {
-                    const int s = i % NS;
-                    const uint32_t ph = (uint32_t)((i / NS) & 1);
+                    const int s = i % NX;
+                    const uint32_t ph = (uint32_t)((i / NX) & 1);
                     const uint32_t aph = (uint32_t)((i / D_LANES) & 1);
-                    if (!wait_or_abort(BAR(full, s), ph, abort_flag, p.status)) break;
-                    if (!wait_or_abort(BAR(a_full, e), aph, abort_flag, p.status)) break;
-                    tc_fence_after();
+                    if (!wait_or_abort(BAR(xfull, s), ph, abort_flag, p.status)) break;
                     const int j = u - seg_start;  // block index within the segment
                     const uint32_t dcol = tmem + D_ACC_COL0 + (uint32_t)(D_LANES * db + e) * D_MMA_N;
                     const uint32_t acol = tmem + (uint32_t)e * D_A_COLS;
-                    const uint64_t bd0 = sw128_desc(base + (uint32_t)s * STAGE + X_OFF);
+                    const uint64_t bd0 = sw128_desc(base + (uint32_t)s * D_X_BYTES);
+                    bool ok = true;
 #pragma unroll
-                    for (int k = 0; k < KBLK / 16; ++k) {
-                        // +32 bytes per 16-deep step, +2 KB per 64-deep panel (descriptor units of 16 bytes)
-                        const uint64_t bd = bd0 + (uint64_t)((k >> 2) * (D_X_PANEL >> 4) + (k & 3) * 2);
-                        umma_ts(dcol, acol + 8u * k, bd, D_IDESC, (j < D_LANES && k == 0) ? 0u : 1u);
+                    for (int h = 0; h < 2; ++h) {  // each half of the depth as soon as it is in TMEM
+                        if (!wait_or_abort(BAR(a_full, 2 * e + h), aph, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 4 * h; k < 4 * h + 4; ++k) {
+                            // +32 bytes per 16-deep step, +2 KB per 64-deep panel (descriptor units of 16 bytes)
+                            const uint64_t bd = bd0 + (uint64_t)((k >> 2) * (D_X_PANEL >> 4) + (k & 3) * 2);
+                            umma_ts(dcol, acol + 8u * k, bd, D_IDESC, (j < D_LANES && k == 0) ? 0u : 1u);
+                        }
+                        umma_commit(BAR(a_empty, 2 * e + h));
                     }
-                    umma_commit(BAR(a_empty, e));
-                    umma_commit(BAR(empty, s));
+                    if (!ok) break;
+                    umma_commit(BAR(xempty, s));
                 }
                 if (seg_end) {
                     umma_commit(BAR(acc_full, db));  // this issuer's MMAs of the segment (maybe none)
@@ -218,35 +265,40 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         const int n_in = 32 * q + lane;           // weight row of this thread within the tile
         const int M = p.M;
         const int tile0 = u0 / KB;
+        pdl_wait();  // y, the partials and the counters may still be in use by the previous kernel
         for (int u = u0 + g, i = g; u < u1; u += D_LANES, i += D_LANES) {
-            const int s = i % NS;
-            const uint32_t ph = (uint32_t)((i / NS) & 1);
+            const int ps = (i >> 1) % NP;  // pair slot of this block
+            const uint32_t ph = (uint32_t)(((i >> 1) / NP) & 1);
             const uint32_t aph = (uint32_t)((i / D_LANES) & 1);
-            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), ph, abort_flag, p.status))) break;
-            const uint32_t st = base + (uint32_t)s * STAGE;
+            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(wfull, ps), ph, abort_flag, p.status))) break;
+            const uint32_t st = wbase + (uint32_t)ps * (2u * BB) + (uint32_t)(i & 1) * BB;
             uint32_t cw[4 * BITS];
             load_row_codes_smem<BITS>(st, n_in, cw);
             uint32_t sbw[sb_words(GROUP)];
             load_row_sb_smem<GROUP>(st + sb_offset(BITS, GROUP, n_in), sbw);
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(empty, s));  // codes are in registers
-            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, g), aph ^ 1u, abort_flag, p.status))) break;
-            tc_fence_after();
+            if (lane == 0) mbar_arrive(BAR(wempty, ps));  // codes are in registers
+            // Each half of the row's depth goes to its own half of the lane's
+            // A buffer, so the MMAs of one half run while the other half is
+            // dequantized (and the next block's first half while this
+            // block's second half is multiplied).
             const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)g * D_A_COLS;
-            {
+            auto half = [&](auto hc) -> bool {
+                constexpr int H = decltype(hc)::value;
                 uint32_t w[32];
-                weight_pairs<BITS, GROUP, 0, 32>(cw, sbw, w);
-                tmem_st32(ta, w);
-            }
-            {
-                uint32_t w[32];
-                weight_pairs<BITS, GROUP, 32, 32>(cw, sbw, w);
-                tmem_st32(ta + 32, w);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(a_full, g));
+                weight_pairs<BITS, GROUP, 32 * H, 32>(cw, sbw, w);
+                if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, 2 * g + H), aph ^ 1u, abort_flag, p.status)))
+                    return false;
+                tc_fence_after();
+                tmem_st32(ta + 32u * H, w);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(a_full, 2 * g + H));
+                return true;
+            };
+            if (!half(std::integral_constant<int, 0>{})) break;
+            if (!half(std::integral_constant<int, 1>{})) break;
 
             // ---- this block ends a tile segment: drain the accumulators
             const int tile = u / KB;
@@ -336,10 +388,15 @@ __global__ void __launch_bounds__(D_THREADS, 1)
 }
 
 template <int BITS, int GROUP>
+size_t dec_smem() {
+    return (size_t)D_XRING * D_X_BYTES + (size_t)dec_wring<BITS, GROUP>() * block_bytes(BITS, GROUP) + sizeof(DecSmem) +
+           1024;
+}
+
+template <int BITS, int GROUP>
 cudaError_t launch_bg(const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    const size_t smem = (size_t)dec_ring<BITS, GROUP>() * dec_stage_bytes<BITS, GROUP>() + sizeof(DecSmem) + 1024;
-    decode_kernel<BITS, GROUP><<<grid, D_THREADS, smem, st>>>(p, map);
-    return cudaGetLastError();
+    const size_t smem = dec_smem<BITS, GROUP>();
+    return launch_pdl(decode_kernel<BITS, GROUP>, grid, D_THREADS, smem, st, p, map);
 }
 
 template <int BITS>
@@ -352,7 +409,7 @@ cudaError_t launch_b(int group, const DecParams& p, const CUtensorMap& map, int 
 template <int BITS, int GROUP>
 cudaError_t allow_bg() {
     return cudaFuncSetAttribute(decode_kernel<BITS, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kDecodeSmemMax);
+                                (int)dec_smem<BITS, GROUP>());
 }
 
 template <int BITS>
@@ -363,11 +420,6 @@ cudaError_t allow_b() {
 }
 
 }  // namespace
-
-size_t decode_smem_bytes(int bits, int group) {
-    const size_t stage = (size_t)(block_bytes(bits, group) + 1023) / 1024 * 1024 + D_X_BYTES;
-    return (size_t)dec_ring_for((uint32_t)stage) * stage + sizeof(DecSmem) + 1024;
-}
 
 cudaError_t decode_allow_smem() {
     for (cudaError_t e : {allow_b<2>(), allow_b<3>(), allow_b<4>(), allow_b<5>(), allow_b<6>(), allow_b<8>()})

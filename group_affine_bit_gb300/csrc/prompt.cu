@@ -5,10 +5,11 @@
 // are the B operand in shared memory.  One CTA per SM works on a contiguous
 // run of units ("stream-K"); a unit is a 256-row tile pair (two 128-row
 // layout tiles) x one 128-deep block.  Per unit:
-//   * a producer thread copies the unit's 128 x 128 activation tile (TMA,
+//   * one producer thread copies the unit's 128 x 128 activation tile (TMA,
 //     two 64-wide panels, 128-byte swizzle, rows past M and depth past K read
-//     as zero) and the two packed weight blocks (one bulk copy each, about
-//     9 KB at 4 bits) into one shared-memory stage of a ring;
+//     as zero) into a ring of activation stages, another the two packed
+//     weight blocks (one bulk copy each, about 9 KB at 4 bits) into a deeper
+//     ring of weight stages;
 //   * two dequantization groups of four warps -- one per 128-row layout
 //     tile, one thread per weight row -- read their row's codes back, round
 //     every weight once as bf16(fma(s, q, b)) (affqmm_format.cuh, the same
@@ -16,9 +17,10 @@
 //     tensor-memory A buffer with tcgen05.st.  Units alternate between two
 //     such pairs of groups, each with its own A buffers, so one unit is
 //     dequantized while the MMAs of the previous one run;
-//   * one thread issues the unit's MMAs (M = 128 weight rows, N = activation
-//     rows rounded up to 16, K = 16): two chains, one per layout tile, each
-//     accumulating over the tile's whole depth in fp32 in tensor memory;
+//   * two threads (one per layout tile) issue the unit's MMAs (M = 128
+//     weight rows, N = activation rows rounded up to 16, K = 16), each into
+//     its own fp32 accumulator in tensor memory over the tile's whole depth
+//     (one issuing thread cannot keep the tensor pipe busy at these sizes);
 //   * at the end of a tile's segment four epilogue warps read the two
 //     accumulators with tcgen05.ld and store bf16 y, or, when several runs
 //     share the tile, an fp32 partial; a second, small kernel then adds each
@@ -44,9 +46,10 @@ namespace affqmm {
 namespace {
 
 constexpr int P_DEQ_GROUPS = 4;                                  // (layout tile, unit parity)
-constexpr int P_DEQ_WARP0 = 2;                                   // warp 0: producer, 1: MMA
-constexpr int P_EPI_WARP0 = P_DEQ_WARP0 + 4 * P_DEQ_GROUPS;      // 18
-constexpr int P_THREADS = (P_EPI_WARP0 + 4) * 32;                // 704
+constexpr int P_DEQ_WARP0 = 3;                                   // warp 0: weights producer, 1-2: MMA issuers
+constexpr int P_EPI_WARP0 = P_DEQ_WARP0 + 4 * P_DEQ_GROUPS;      // 19
+constexpr int P_XPROD = P_EPI_WARP0 + 4;                         // 23: activations producer
+constexpr int P_THREADS = (P_XPROD + 1) * 32;                    // 768
 constexpr int P_TILE_N = 256;                                    // weight rows per unit
 constexpr int P_ROWS = 128;                                      // activation rows per launch (max)
 constexpr uint32_t P_X_PANEL = P_ROWS * 128;                     // 128 rows x 64 k bf16, 16 KB
@@ -58,8 +61,10 @@ constexpr uint32_t P_A_COLS = KBLK / 2;                          // 128 bf16 per
 constexpr int P_RING_MAX = 8;
 
 struct PromptSmem {
-    uint64_t full[P_RING_MAX];
-    uint64_t empty[P_RING_MAX];
+    uint64_t xfull[P_RING_MAX];
+    uint64_t xempty[P_RING_MAX];
+    uint64_t wfull[P_RING_MAX];
+    uint64_t wempty[P_RING_MAX];
     uint64_t a_full[P_DEQ_GROUPS];
     uint64_t a_empty[P_DEQ_GROUPS];
     uint64_t acc_full;
@@ -68,20 +73,34 @@ struct PromptSmem {
     int abort_flag;
 };
 
-// A stage: the activation block (1024-byte aligned for the swizzle), then the
-// unit's two packed weight blocks.
+// Two rings in shared memory: activation blocks (32 KB each, 1024-byte
+// aligned for the swizzle; held until the unit's MMAs are done) and packed
+// weight blocks (the unit's two blocks; held only until the dequantization
+// warps have read them, so that ring runs further ahead of the HBM latency).
+// The weight ring has an even depth: its stage s always serves units of
+// parity s mod 2, whose dequantization groups are the only readers.
+constexpr uint32_t kPromptSmemBudget = 210u * 1024u;
 template <int BITS, int GROUP>
-constexpr uint32_t prm_stage_bytes() {
-    return (P_X_BYTES + 2u * (uint32_t)block_bytes(BITS, GROUP) + 1023u) / 1024u * 1024u;
-}
-// As many stages as fit in ~200 KB, an even number (stage s always serves
-// units of parity s mod 2, so every barrier has one set of waiters).
-constexpr int prm_ring_for(uint32_t stage) {
-    return (int)(200u * 1024u / stage) / 2 * 2 > P_RING_MAX ? P_RING_MAX : (int)(200u * 1024u / stage) / 2 * 2;
+constexpr uint32_t prm_wstage() {
+    return 2u * (uint32_t)block_bytes(BITS, GROUP);
 }
 template <int BITS, int GROUP>
-constexpr int prm_ring() {
-    return prm_ring_for(prm_stage_bytes<BITS, GROUP>());
+constexpr int prm_wring_for(int nx) {
+    return (int)((kPromptSmemBudget - (uint32_t)nx * P_X_BYTES) / prm_wstage<BITS, GROUP>()) / 2 * 2 > P_RING_MAX
+               ? P_RING_MAX
+               : (int)((kPromptSmemBudget - (uint32_t)nx * P_X_BYTES) / prm_wstage<BITS, GROUP>()) / 2 * 2;
+}
+template <int BITS, int GROUP>
+constexpr int prm_xring() {  // activations come from L2 but wait for the MMAs: as deep as leaves 2 weight stages
+    return prm_wring_for<BITS, GROUP>(4) >= 2 ? 4 : prm_wring_for<BITS, GROUP>(3) >= 2 ? 3 : 2;
+}
+template <int BITS, int GROUP>
+constexpr int prm_wring() {
+    return prm_wring_for<BITS, GROUP>(prm_xring<BITS, GROUP>());
+}
+template <int BITS, int GROUP>
+constexpr size_t prm_ring_bytes() {
+    return (size_t)prm_xring<BITS, GROUP>() * P_X_BYTES + (size_t)prm_wring<BITS, GROUP>() * prm_wstage<BITS, GROUP>();
 }
 
 template <int BITS, int GROUP>
@@ -89,14 +108,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     prompt_kernel(const __grid_constant__ PromptParams p, const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int BB = block_bytes(BITS, GROUP);
-    constexpr uint32_t STAGE = prm_stage_bytes<BITS, GROUP>();
-    constexpr int NS = prm_ring<BITS, GROUP>();
-    static_assert(NS >= 2 && NS % 2 == 0, "ring depth");
+    constexpr int NX = prm_xring<BITS, GROUP>();
+    constexpr int NW = prm_wring<BITS, GROUP>();
+    constexpr uint32_t WSTAGE = prm_wstage<BITS, GROUP>();
+    static_assert(NX >= 2 && NW >= 2 && NW % 2 == 0, "ring depths");
     static_assert(BB % 16 == 0, "bulk copies move multiples of 16 bytes");
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    PromptSmem* sh = reinterpret_cast<PromptSmem*>(smem_raw + (base - raw) + (size_t)NS * STAGE);
-    const uint32_t sh_addr = base + (uint32_t)NS * STAGE;
+    const uint32_t base = (raw + 1023u) & ~1023u;        // activation ring
+    const uint32_t wbase = base + (uint32_t)NX * P_X_BYTES;  // weight ring
+    PromptSmem* sh = reinterpret_cast<PromptSmem*>(smem_raw + (base - raw) + prm_ring_bytes<BITS, GROUP>());
+    const uint32_t sh_addr = base + (uint32_t)prm_ring_bytes<BITS, GROUP>();
 #define BAR(field, i) (sh_addr + (uint32_t)offsetof(PromptSmem, field) + 8u * (uint32_t)(i))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -110,15 +131,19 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const int u1 = (int)((int64_t)(c + 1) * U / PC);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(BAR(full, s), 1);
-            mbar_init(BAR(empty, s), 9);  // the 8 warps that read the packed blocks, and the MMAs that read x
+        for (int s = 0; s < NX; ++s) {
+            mbar_init(BAR(xfull, s), 1);
+            mbar_init(BAR(xempty, s), 2);  // the two issuers' MMAs read the activations
+        }
+        for (int s = 0; s < NW; ++s) {
+            mbar_init(BAR(wfull, s), 1);
+            mbar_init(BAR(wempty, s), 8);  // the 8 dequantization warps of the unit read the packed blocks
         }
         for (int g = 0; g < P_DEQ_GROUPS; ++g) {
             mbar_init(BAR(a_full, g), 4);
             mbar_init(BAR(a_empty, g), 1);
         }
-        mbar_init(BAR(acc_full, 0), 1);
+        mbar_init(BAR(acc_full, 0), 2);   // both issuers commit at every segment end
         mbar_init(BAR(acc_empty, 0), 4);  // one arrival per epilogue warp
         sh->abort_flag = 0;
         fence_mbar_init();
@@ -129,33 +154,50 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort_flag = &sh->abort_flag;
+    if (threadIdx.x == 0) pdl_launch_dependents();
 
     if (warp == 0) {
-        // ---------------------------------------------------------- producer
+        // ---------------------------------------------------------- weights producer
         if (lane == 0) {
-            prefetch_tmap(&xmap);
             const uint64_t policy = policy_evict_first();  // the weights are read once
             for (int u = u0, i = 0; u < u1; ++u, ++i) {
-                const int s = i % NS;
-                const uint32_t ph = (uint32_t)((i / NS) & 1);
-                if (!wait_or_abort(BAR(empty, s), ph ^ 1u, abort_flag, p.status)) break;
+                const int s = i % NW;
+                const uint32_t ph = (uint32_t)((i / NW) & 1);
+                if (!wait_or_abort_lazy(BAR(wempty, s), ph ^ 1u, abort_flag, p.status)) break;
                 const int tile = u / KB, kb = u - (u / KB) * KB;
                 const int lt0 = 2 * tile;
                 const bool two = lt0 + 1 < P.ltiles;
-                const uint32_t st = base + (uint32_t)s * STAGE;
-                mbar_arrive_expect_tx(BAR(full, s), P_X_BYTES + (two ? 2u : 1u) * (uint32_t)BB);
-                tma_load_2d(st, &xmap, kb * KBLK, 0, BAR(full, s));
-                tma_load_2d(st + P_X_PANEL, &xmap, kb * KBLK + 64, 0, BAR(full, s));
-                bulk_g2s_hint(st + P_X_BYTES, P.packed + ((size_t)lt0 * KB + kb) * BB, (uint32_t)BB, BAR(full, s),
-                              policy);
+                const uint32_t st = wbase + (uint32_t)s * WSTAGE;
+                mbar_arrive_expect_tx(BAR(wfull, s), (two ? 2u : 1u) * (uint32_t)BB);
+                bulk_g2s_hint(st, P.packed + ((size_t)lt0 * KB + kb) * BB, (uint32_t)BB, BAR(wfull, s), policy);
                 if (two)
-                    bulk_g2s_hint(st + P_X_BYTES + (uint32_t)BB, P.packed + ((size_t)(lt0 + 1) * KB + kb) * BB,
-                                  (uint32_t)BB, BAR(full, s), policy);
+                    bulk_g2s_hint(st + (uint32_t)BB, P.packed + ((size_t)(lt0 + 1) * KB + kb) * BB, (uint32_t)BB,
+                                  BAR(wfull, s), policy);
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp == P_XPROD) {
+        // ---------------------------------------------------------- activations producer
         if (lane == 0) {
+            prefetch_tmap(&xmap);
+            pdl_wait();  // x may come from the previous kernel
+            int kb = u0 % KB;
+            for (int u = u0, i = 0; u < u1; ++u, ++i) {
+                const int s = i % NX;
+                const uint32_t ph = (uint32_t)((i / NX) & 1);
+                if (!wait_or_abort_lazy(BAR(xempty, s), ph ^ 1u, abort_flag, p.status)) break;
+                const uint32_t st = base + (uint32_t)s * P_X_BYTES;
+                mbar_arrive_expect_tx(BAR(xfull, s), P_X_BYTES);
+                tma_load_2d(st, &xmap, kb * KBLK, 0, BAR(xfull, s));
+                tma_load_2d(st + P_X_PANEL, &xmap, kb * KBLK + 64, 0, BAR(xfull, s));
+                if (++kb == KB) kb = 0;
+            }
+        }
+    } else if (warp < P_DEQ_WARP0) {
+        // ---------------------------------------------------------- MMA issuers
+        // issuer `sub` accumulates layout tile `sub` of every unit (one
+        // issuing thread per accumulator keeps the fp32 order fixed)
+        if (lane == 0) {
+            const int sub = warp - 1;
             const int nn = p.M <= 16 ? 16 : (p.M + 15) / 16 * 16;  // MMA N: activation rows
             const uint32_t idesc = idesc_bf16_f32(128, nn);
             int seg = 0;
@@ -167,29 +209,25 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     tc_fence_after();
                     open = first = true;
                 }
-                const int s = i % NS;
-                const uint32_t ph = (uint32_t)((i / NS) & 1);
+                const int s = i % NX;
+                const uint32_t ph = (uint32_t)((i / NX) & 1);
                 const int par = i & 1;
                 const uint32_t aph = (uint32_t)((i >> 1) & 1);
-                if (!wait_or_abort(BAR(full, s), ph, abort_flag, p.status)) break;
-                if (!wait_or_abort(BAR(a_full, par), aph, abort_flag, p.status)) break;
-                if (!wait_or_abort(BAR(a_full, 2 + par), aph, abort_flag, p.status)) break;
+                if (!wait_or_abort(BAR(xfull, s), ph, abort_flag, p.status)) break;
+                if (!wait_or_abort(BAR(a_full, 2 * sub + par), aph, abort_flag, p.status)) break;
                 tc_fence_after();
-                const uint64_t bd0 = sw128_desc(base + (uint32_t)s * STAGE);
+                const uint64_t bd0 = sw128_desc(base + (uint32_t)s * P_X_BYTES);
+                const uint32_t dcol = tmem + (uint32_t)sub * P_ACC_COLS;
+                const uint32_t acol = tmem + P_A_COL0 + (uint32_t)(2 * sub + par) * P_A_COLS;
 #pragma unroll
                 for (int k = 0; k < KBLK / 16; ++k) {
                     // +32 bytes per 16-deep step, +16 KB per 64-deep panel (descriptor units of 16 bytes)
                     const uint64_t bd = bd0 + (uint64_t)((k >> 2) * (P_X_PANEL >> 4) + (k & 3) * 2);
-                    const uint32_t acc = (first && k == 0) ? 0u : 1u;
-#pragma unroll
-                    for (int sub = 0; sub < 2; ++sub)
-                        umma_ts(tmem + (uint32_t)sub * P_ACC_COLS,
-                                tmem + P_A_COL0 + (uint32_t)(2 * sub + par) * P_A_COLS + 8u * k, bd, idesc, acc);
+                    umma_ts(dcol, acol + 8u * k, bd, idesc, (first && k == 0) ? 0u : 1u);
                 }
                 first = false;
-                umma_commit(BAR(a_empty, par));
-                umma_commit(BAR(a_empty, 2 + par));
-                umma_commit(BAR(empty, s));
+                umma_commit(BAR(a_empty, 2 * sub + par));
+                umma_commit(BAR(xempty, s));
                 if (kb == KB - 1 || u == u1 - 1) {
                     umma_commit(BAR(acc_full, 0));
                     ++seg;
@@ -208,16 +246,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         const int q = warp & 3;
         const int n_in = 32 * q + lane;
         for (int u = u0 + par, i = par; u < u1; u += 2, i += 2) {
-            const int s = i % NS;
-            const uint32_t ph = (uint32_t)((i / NS) & 1);
+            const int s = i % NW;
+            const uint32_t ph = (uint32_t)((i / NW) & 1);
             const uint32_t aph = (uint32_t)((i >> 1) & 1);
-            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), ph, abort_flag, p.status))) break;
+            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(wfull, s), ph, abort_flag, p.status))) break;
             const int tile = u / KB;
             const bool present = 2 * tile + sub < P.ltiles;
             uint32_t cw[4 * BITS];
             uint32_t sbw[sb_words(GROUP)];
             if (present) {
-                const uint32_t blk = base + (uint32_t)s * STAGE + P_X_BYTES + (uint32_t)(sub * BB);
+                const uint32_t blk = wbase + (uint32_t)s * WSTAGE + (uint32_t)(sub * BB);
                 load_row_codes_smem<BITS>(blk, n_in, cw);
                 load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, n_in), sbw);
             } else {  // rows past the last layout tile: zero weights
@@ -227,7 +265,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 for (int w = 0; w < sb_words(GROUP); ++w) sbw[w] = 0u;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(empty, s));  // codes are in registers
+            if (lane == 0) mbar_arrive(BAR(wempty, s));  // codes are in registers
             uint32_t w[32];
             weight_pairs<BITS, GROUP, 0, 32>(cw, sbw, w);
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, abuf), aph ^ 1u, abort_flag, p.status))) break;
@@ -248,6 +286,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         const int n_in = 32 * q + lane;
         const int M = p.M;
         const int nchunks = (M + 31) / 32;    // 32-column pieces of the accumulators to read
+        pdl_wait();  // y and the partial slots may still be in use by the previous kernel
         int seg = 0;
         int seg_start = u0;
         for (int u = u0; u < u1; ++u) {
@@ -341,13 +380,12 @@ __global__ void __launch_bounds__(P_TILE_N) prompt_merge_kernel(const __grid_con
 
 template <int BITS, int GROUP>
 size_t prompt_smem_for() {
-    return (size_t)prm_ring<BITS, GROUP>() * prm_stage_bytes<BITS, GROUP>() + sizeof(PromptSmem) + 1024;
+    return prm_ring_bytes<BITS, GROUP>() + sizeof(PromptSmem) + 1024;
 }
 
 template <int BITS, int GROUP>
 cudaError_t launch_prompt_bg(const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    prompt_kernel<BITS, GROUP><<<grid, P_THREADS, prompt_smem_for<BITS, GROUP>(), st>>>(p, map);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(prompt_kernel<BITS, GROUP>, grid, P_THREADS, prompt_smem_for<BITS, GROUP>(), st, p, map);
     if (e != cudaSuccess) return e;
     const PromptProj& last = p.proj[p.nproj - 1];
     const dim3 mgrid((unsigned)(last.ctr_begin + last.tiles), (unsigned)((p.M + 15) / 16));
