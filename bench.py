@@ -42,8 +42,9 @@ if ROOT not in sys.path:
 
 METRIC = "affine-4bit qmm packed-weight GB/s vs HBM peak (M=1..16); TFLOP/s at M=128"
 L2_BYTES = 129 * 10 ** 6
-KERNEL_SOURCES = ["group_affine_bit_gb300/csrc/decode.cu", "group_affine_bit_gb300/csrc/affqmm_format.cuh",
-                  "group_affine_bit_gb300/csrc/prompt.cu"]
+KERNEL_SOURCES = ["group_affine_bit_gb300/csrc/decode.cu", "group_affine_bit_gb300/csrc/prompt.cu",
+                  "group_affine_bit_gb300/csrc/affqmm_format.cuh", "group_affine_bit_gb300/csrc/affqmm_tc.cuh",
+                  "group_affine_bit_gb300/csrc/affqmm_async.cuh"]
 
 
 # ----------------------------------------------------------------------------- setup
