@@ -87,10 +87,10 @@ constexpr size_t kPromptSlotFloats = 128 * 256;
 // the previous kernel in the stream finishes, and resolves the dependency
 // itself (griddepcontrol.wait) before it touches data that kernel may use.
 template <typename... Params, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Params...), int grid, int threads, size_t smem, cudaStream_t st,
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, int threads, size_t smem, cudaStream_t st,
                        Args&&... args) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;

@@ -59,7 +59,9 @@ constexpr int D_MMA_N = 16;           // activation rows per MMA (M <= 16)
 constexpr uint32_t D_X_PANEL = D_MMA_N * 128;      // 16 rows x 64 k bf16, 2 KB
 constexpr uint32_t D_X_BYTES = 2 * D_X_PANEL;      // one 128-deep block of x
 constexpr uint32_t D_TMEM_COLS = 512;
-constexpr uint32_t D_A_COLS = KBLK / 2;            // 64 columns: 128 bf16 per row
+constexpr int D_A_HALVES = 3;                      // A buffers per lane, each half a block deep
+constexpr uint32_t D_A_HALF_COLS = KBLK / 4;        // 32 columns: 64 bf16 per row
+constexpr uint32_t D_A_COLS = D_A_HALVES * D_A_HALF_COLS;  // 96 columns per lane
 constexpr uint32_t D_ACC_COL0 = D_LANES * D_A_COLS;
 // Accumulators: one chain per lane of work (its blocks of the segment), and
 // two segments' worth so the next segment starts while the last one is
@@ -79,8 +81,8 @@ struct DecSmem {
     uint64_t wempty[D_WRING_MAX];
     uint64_t xfull[D_XRING];
     uint64_t xempty[D_XRING];
-    uint64_t a_full[2 * D_LANES];   // (lane, half of the block's depth)
-    uint64_t a_empty[2 * D_LANES];
+    uint64_t a_full[D_A_HALVES * D_LANES];   // (lane, A buffer)
+    uint64_t a_empty[D_A_HALVES * D_LANES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             mbar_init(BAR(xfull, s), 1);
             mbar_init(BAR(xempty, s), 1);  // the block's MMAs read x
         }
-        for (int l = 0; l < 2 * D_LANES; ++l) {
+        for (int l = 0; l < D_A_HALVES * D_LANES; ++l) {
             mbar_init(BAR(a_full, l), 4);
             mbar_init(BAR(a_empty, l), 1);
         }
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
                 if ((i & (D_LANES - 1)) == e) {
                     const int s = i % NX;
                     const uint32_t ph = (uint32_t)((i / NX) & 1);
-                    const uint32_t aph = (uint32_t)((i / D_LANES) & 1);
+                    const int jl = i / D_LANES;  // this lane's block count; its halves are 2 jl, 2 jl + 1
                     if (!wait_or_abort(BAR(xfull, s), ph, abort_flag, p.status)) break;
                     const int j = u - seg_start;  // block index within the segment
                     const uint32_t dcol = tmem + D_ACC_COL0 + (uint32_t)(D_LANES * db + e) * D_MMA_N;
@@ -233,7 +235,10 @@ __global__ void __launch_bounds__(D_THREADS, 1)
                     bool ok = true;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {  // each half of the depth as soon as it is in TMEM
-                        if (!wait_or_abort(BAR(a_full, 2 * e + h), aph, abort_flag, p.status)) {
+                        const int t = 2 * jl + h;  // the lane's half number: buffer t mod 3, use t / 3
+                        const int b = t % D_A_HALVES;
+                        if (!wait_or_abort(BAR(a_full, D_A_HALVES * e + b), (uint32_t)((t / D_A_HALVES) & 1), abort_flag,
+                                           p.status)) {
                             ok = false;
                             break;
                         }
@@ -242,9 +247,10 @@ __global__ void __launch_bounds__(D_THREADS, 1)
                         for (int k = 4 * h; k < 4 * h + 4; ++k) {
                             // +32 bytes per 16-deep step, +2 KB per 64-deep panel (descriptor units of 16 bytes)
                             const uint64_t bd = bd0 + (uint64_t)((k >> 2) * (D_X_PANEL >> 4) + (k & 3) * 2);
-                            umma_ts(dcol, acol + 8u * k, bd, D_IDESC, (j < D_LANES && k == 0) ? 0u : 1u);
+                            umma_ts(dcol, acol + (uint32_t)b * D_A_HALF_COLS + 8u * (k - 4 * h), bd, D_IDESC,
+                                    (j < D_LANES && k == 0) ? 0u : 1u);
                         }
-                        umma_commit(BAR(a_empty, 2 * e + h));
+                        umma_commit(BAR(a_empty, D_A_HALVES * e + b));
                     }
                     if (!ok) break;
                     umma_commit(BAR(xempty, s));
@@ -269,7 +275,6 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         for (int u = u0 + g, i = g; u < u1; u += D_LANES, i += D_LANES) {
             const int ps = (i >> 1) % NP;  // pair slot of this block
             const uint32_t ph = (uint32_t)(((i >> 1) / NP) & 1);
-            const uint32_t aph = (uint32_t)((i / D_LANES) & 1);
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(wfull, ps), ph, abort_flag, p.status))) break;
             const uint32_t st = wbase + (uint32_t)ps * (2u * BB) + (uint32_t)(i & 1) * BB;
             uint32_t cw[4 * BITS];
@@ -278,23 +283,25 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             load_row_sb_smem<GROUP>(st + sb_offset(BITS, GROUP, n_in), sbw);
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(wempty, ps));  // codes are in registers
-            // Each half of the row's depth goes to its own half of the lane's
-            // A buffer, so the MMAs of one half run while the other half is
-            // dequantized (and the next block's first half while this
-            // block's second half is multiplied).
+            // Each half of the row's depth goes to the next of the lane's three
+            // half-block A buffers, so the dequantization runs up to a block
+            // and a half ahead of the lane's MMAs.
             const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)g * D_A_COLS;
             auto half = [&](auto hc) -> bool {
                 constexpr int H = decltype(hc)::value;
                 uint32_t w[32];
                 weight_pairs<BITS, GROUP, 32 * H, 32>(cw, sbw, w);
-                if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, 2 * g + H), aph ^ 1u, abort_flag, p.status)))
+                const int t = 2 * (i / D_LANES) + H;  // the lane's half number: buffer t mod 3, use t / 3
+                const int b = t % D_A_HALVES;
+                if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, D_A_HALVES * g + b),
+                                                           (uint32_t)((t / D_A_HALVES) & 1) ^ 1u, abort_flag, p.status)))
                     return false;
                 tc_fence_after();
-                tmem_st32(ta + 32u * H, w);
+                tmem_st32(ta + (uint32_t)b * D_A_HALF_COLS, w);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(a_full, 2 * g + H));
+                if (lane == 0) mbar_arrive(BAR(a_full, D_A_HALVES * g + b));
                 return true;
             };
             if (!half(std::integral_constant<int, 0>{})) break;

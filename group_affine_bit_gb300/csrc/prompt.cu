@@ -348,6 +348,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 // activation rows); thread = one of the tile's 256 weight rows.  Tiles that
 // one run owned were stored by prompt_kernel and are skipped.
 __global__ void __launch_bounds__(P_TILE_N) prompt_merge_kernel(const __grid_constant__ PromptParams p) {
+    pdl_launch_dependents();  // the next kernel's prologue and weight copies may start
+    pdl_wait();               // the partials of prompt_kernel are complete and visible
     const int t_all = (int)blockIdx.x;
     int pi = 0;
     for (int i = 1; i < p.nproj; ++i)
@@ -389,8 +391,7 @@ cudaError_t launch_prompt_bg(const PromptParams& p, const CUtensorMap& map, int 
     if (e != cudaSuccess) return e;
     const PromptProj& last = p.proj[p.nproj - 1];
     const dim3 mgrid((unsigned)(last.ctr_begin + last.tiles), (unsigned)((p.M + 15) / 16));
-    prompt_merge_kernel<<<mgrid, P_TILE_N, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(prompt_merge_kernel, mgrid, P_TILE_N, 0, st, p);
 }
 
 template <int BITS>
