@@ -65,6 +65,9 @@ class Oracle:
         lib.oracle_qmm_groupsum.restype = ctypes.c_int
         lib.oracle_qmm_groupsum.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64,
                                             _u16p, _u8p, _u16p, _u16p, _f64p, _f64p]
+        lib.oracle_embed_rows.restype = ctypes.c_int
+        lib.oracle_embed_rows.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _u8p, _u16p, _u16p,
+                                          ctypes.POINTER(ctypes.c_int32), _i64, ctypes.c_int, ctypes.c_uint16, _u16p]
         self.lib = lib
 
     # -- bf16 -----------------------------------------------------------
@@ -129,6 +132,24 @@ class Oracle:
         if rc:
             raise ValueError(f"oracle_qmm_groupsum rejected its arguments (rc={rc})")
         return y, mag
+
+    # -- scaled embedding rows -------------------------------------------------
+    def embed_rows(self, bits, group, codes, scales, biases, ids, scale=None) -> np.ndarray:
+        """out[t,k] = bf16(bf16(s*q + b) * scale) of table row ids[t]; scale is a
+        bf16 bit pattern, or None for the weight row itself."""
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        biases = np.ascontiguousarray(biases, dtype=np.uint16)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        N, K = codes.shape
+        T = ids.shape[0]
+        out = np.empty((T, K), dtype=np.uint16)
+        rc = self.lib.oracle_embed_rows(bits, group, N, K, _ptr(codes, _u8p), _ptr(scales, _u16p),
+                                        _ptr(biases, _u16p), ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), T,
+                                        0 if scale is None else 1, 0 if scale is None else int(scale), _ptr(out, _u16p))
+        if rc:
+            raise ValueError(f"oracle_embed_rows rejected its arguments (rc={rc})")
+        return out
 
 
 _DEFAULT = None

@@ -13,6 +13,9 @@
  *   3. the projection y[m,n] = sum_k W[n,k] * x[m,k] over the whole depth in
  *      double (the pages' tensor unit accumulates over the whole depth; the
  *      oracle's float64 sum stands for the exact sum).
+ *   4. scaled embedding rows bf16(W[n,k] * scale) -- "cuda gemma4: images on
+ *      the 12B" page, the embed_rows commit (the weight rounded first, then
+ *      its product with the bf16 scale rounded again).
  *
  * The arithmetic is deliberately plain: no blocking, no vectorization, no
  * reordering of the sum.  Threads only split independent output rows.
@@ -231,6 +234,32 @@ int oracle_qmm_groupsum(int bits, int group, int64_t M, int64_t N, int64_t K,
             }
             if (y_gs) y_gs[m * N + n] = acc;
             if (mag) mag[m * N + n] = amag;
+        }
+    }
+    return 0;
+}
+
+int oracle_embed_rows(int bits, int group, int64_t N, int64_t K,
+                      const uint8_t* codes, const uint16_t* scales,
+                      const uint16_t* biases, const int32_t* ids, int64_t T,
+                      int has_scale, uint16_t scale, uint16_t* out) {
+    int rc = check_args(bits, group, N, K);
+    if (rc) return rc;
+    if (T < 0) return -3;
+    const int64_t G = K / group;
+    const uint32_t qmax = (1u << bits) - 1u;
+    const double sc = oracle_bf16_to_double(scale);
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t n = ids[t];
+        if (n < 0 || n >= N) return -6;
+        for (int64_t k = 0; k < K; ++k) {
+            uint32_t q = codes[n * K + k];
+            if (q > qmax) return -4;
+            int64_t j = k / group;
+            uint16_t w = oracle_dequant_one(q, scales[n * G + j], biases[n * G + j]);
+            /* Two bf16 values have 8 significant bits each, so their product is
+             * exact in double and this is its single rounding. */
+            out[t * K + k] = has_scale ? oracle_bf16_from_double(oracle_bf16_to_double(w) * sc) : w;
         }
     }
     return 0;

@@ -71,6 +71,17 @@ int oracle_qmm_groupsum(int bits, int group, int64_t M, int64_t N, int64_t K,
                         const uint16_t* scales, const uint16_t* biases,
                         double* y_gs, double* mag);
 
+/* Scaled embedding rows: out[t,k] = bf16( bf16(s*q + b) * scale ) for the
+ * table row n = ids[t] -- two roundings, each of an exact value: the weight
+ * (as oracle_dequant_one) and then its exact product with the bf16 scale.
+ * "cuda gemma4: images on the 12B" page, the embed_rows commit.  has_scale = 0
+ * gives the weight row itself (no second rounding).  out is [T,K] row-major.
+ * Returns -6 if an id is outside [0, N). */
+int oracle_embed_rows(int bits, int group, int64_t N, int64_t K,
+                      const uint8_t* codes, const uint16_t* scales,
+                      const uint16_t* biases, const int32_t* ids, int64_t T,
+                      int has_scale, uint16_t scale, uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif

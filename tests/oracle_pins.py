@@ -329,6 +329,50 @@ def pin_group_sum_identity(orc, seed=17):
         assert np.max(dev / mag) > 0
 
 
+def _embed_exact_bits(orc_w_bits: int, scale_bits: int) -> int:
+    """bf16(w * scale) from the exact product (w, scale finite bf16 patterns)."""
+    w, sc = bf16_value(orc_w_bits), bf16_value(scale_bits)
+    if isinstance(w, float) or isinstance(sc, float):
+        raise ValueError("finite values only")
+    prod = w * sc
+    neg_zero = prod == 0 and ((orc_w_bits >> 15) ^ (scale_bits >> 15)) == 1
+    return rne_bf16_bits(prod, negative_zero=neg_zero)
+
+
+def pin_embed_rows_exact(orc, seed=19):
+    """Scaled embedding rows against exact arithmetic: each output is the exact
+    product of the exactly rounded weight and the scale, rounded once; the
+    weight is the exact bf16(s*q + b) (two roundings in all, no fewer)."""
+    rng = np.random.default_rng(seed)
+    hidden = rne_bf16_bits(Fraction(math.sqrt(5376)))          # bf16(sqrt(hidden)), Gemma's embedding scale
+    for bits, group, N, K in [(4, 64, 9, 128), (3, 32, 5, 96), (8, 128, 4, 256), (2, 32, 6, 64)]:
+        _, codes, s, b = _small_problem(rng, bits, group, 1, N, K)
+        ids = rng.integers(0, N, 7).astype(np.int32)
+        ids[0] = N - 1
+        for scale in (hidden, 0x3F80, 0x4180, 0xC0A0, 0x3DCD):   # sqrt(5376), 1, 16, -5, ~0.1
+            out = orc.embed_rows(bits, group, codes, s, b, ids, scale)
+            for t, n in enumerate(ids):
+                for k in range(0, K, max(1, K // 24)):
+                    wb = exact_dequant_bits(int(codes[n, k]), int(s[n, k // group]), int(b[n, k // group]))
+                    assert int(out[t, k]) == _embed_exact_bits(wb, scale), (bits, t, k, hex(scale))
+
+
+def pin_embed_rows_special_cases(orc, seed=23):
+    """No scale gives the dequantized rows; scale 1 gives them too; a power-of-two
+    scale multiplies exactly (no overflow or underflow at these magnitudes)."""
+    rng = np.random.default_rng(seed)
+    for bits, group, N, K in [(4, 64, 8, 256), (6, 32, 4, 128)]:
+        _, codes, s, b = _small_problem(rng, bits, group, 1, N, K)
+        W = orc.dequant(bits, group, codes, s, b)
+        ids = np.arange(N, dtype=np.int32)[::-1].copy()
+        assert np.array_equal(orc.embed_rows(bits, group, codes, s, b, ids, None), W[ids])
+        assert np.array_equal(orc.embed_rows(bits, group, codes, s, b, ids, 0x3F80), W[ids])
+        out = orc.embed_rows(bits, group, codes, s, b, ids, 0x4100)   # 8.0
+        for t, n in enumerate(ids):
+            for k in range(K):
+                assert bf16_value(int(out[t, k])) == 8 * bf16_value(int(W[n, k]))
+
+
 ALL_PINS = [
     pin_bf16_golden,
     pin_bf16_against_torch,
@@ -339,4 +383,6 @@ ALL_PINS = [
     pin_one_hot_rows,
     pin_constant_code_groups,
     pin_group_sum_identity,
+    pin_embed_rows_exact,
+    pin_embed_rows_special_cases,
 ]

@@ -53,6 +53,17 @@ PLANTS = {
     # the bias enters with the wrong sign
     "bias_sign": ("double hi = p + bd;\n    double bv = hi - p;",
                   "double hi = p - bd;\n    double bv = hi - p;"),
+    # embedding rows: the scale applied to the unrounded weight (one rounding instead of two)
+    "embed_no_first_rounding": (
+        "out[t * K + k] = has_scale ? oracle_bf16_from_double(oracle_bf16_to_double(w) * sc) : w;",
+        "out[t * K + k] = has_scale ? oracle_bf16_from_double((oracle_bf16_to_double(scales[n * G + j]) * (double)q + "
+        "oracle_bf16_to_double(biases[n * G + j])) * sc) : w;"),
+    # embedding rows: the scale folded into the group's scale and bias
+    "embed_scale_folded": (
+        "uint16_t w = oracle_dequant_one(q, scales[n * G + j], biases[n * G + j]);",
+        "uint16_t w = has_scale ? oracle_dequant_one(q, oracle_bf16_from_double(oracle_bf16_to_double(scales[n * G + j]) * sc), "
+        "oracle_bf16_from_double(oracle_bf16_to_double(biases[n * G + j]) * sc)) : "
+        "oracle_dequant_one(q, scales[n * G + j], biases[n * G + j]); if (has_scale) { out[t * K + k] = w; continue; }"),
     # the scale and bias patterns swapped
     "swapped_scale_bias": ("double sd = oracle_bf16_to_double(s);\n    double bd = oracle_bf16_to_double(b);",
                            "double sd = oracle_bf16_to_double(b);\n    double bd = oracle_bf16_to_double(s);"),
