@@ -11,6 +11,7 @@ over one batch of synthetic input with the weights resident in HBM:
   prompt_chunk              M=128 through one layer's four projection shapes
   lane_sweep                M in {2,4,8,16} at 4-bit g64 and M=16 at 8b/3b/2b
   tiny                      M=1, K=256, N=512, 4-bit g64
+  embed_rows                4096 scaled embedding rows gathered from the tied head's table
 
 `value` is packed-weight bytes (codes + bf16 scales + biases) per second for
 the decode workloads and TFLOP/s for the prompt chunk.  Weight copies rotate
@@ -54,7 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default: per workload)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="gate_up_decode",
-                    choices=["gate_up_decode", "decode_step", "prompt_chunk", "lane_sweep", "tiny"])
+                    choices=["gate_up_decode", "decode_step", "prompt_chunk", "lane_sweep", "tiny", "embed_rows"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -389,8 +390,59 @@ class LaneSweep(Workload):
         return f"{self.name}: K=3840 N=15360, (M, bits, group) in {[(c.M, c.bits, c.group) for c in self.cases]}"
 
 
+class EmbedRows(Workload):
+    """Scaled embedding rows: 4096 token ids gathered from the tied head's table
+    (262144 x 5376, 4-bit g64) times bf16(sqrt(5376)).  Bytes = the gathered
+    rows' packed bytes + the ids + the bf16 output."""
+    name = "embed_rows"
+    default_steps = 500
+    T = 4096
+
+    def make_cases(self, api, synth, device):
+        import torch
+        N, K = synth.HEAD_SHAPE
+        g = synth.generator(synth.EMBED_SEED, device)
+        codes, s, b = synth.affine_table(4, 64, N, K, g, device)
+        self.w = api.pack(codes, s, b, 4, 64)
+        del codes, s, b
+        self.ids = torch.randint(0, N, (self.T,), generator=g, device=device, dtype=torch.int32)
+        self.out = torch.empty(self.T, K, dtype=torch.bfloat16, device=device)
+        self.N, self.K = N, K
+        return []
+
+    def step(self, i: int):
+        self.api.embed_rows(self.w, self.ids, math.sqrt(5376.0), out=self.out)
+
+    launches_per_step = 1
+
+    @property
+    def packed_row_bytes(self) -> int:
+        return self.K * 4 // 8 + 4 * self.K // 64
+
+    @property
+    def units_per_step(self) -> float:
+        return float(self.T * (self.packed_row_bytes + 4 + 2 * self.K))
+
+    def roofline_info(self):
+        return dict(kernel="embed_kernel<4,64>", bound="hbm", units_per_step=self.units_per_step, unit="GB/s",
+                    traffic_key=f"embed {self.name}")
+
+    def l2_note(self) -> str:
+        return "inputs larger than L2: 4096 random rows of a 1.5 GB packed table, 44 MB written per step"
+
+    def describe(self):
+        return f"{self.name}: T={self.T} ids into {self.N}x{self.K} 4-bit g64, scale bf16(sqrt(5376))"
+
+    def config(self):
+        return {"workload": self.describe(), "T": self.T, "N": self.N, "K": self.K, "bits": 4, "group": 64,
+                "l2": self.l2_note(), "parallelism": "replicas"}
+
+    def e2e_io(self):
+        return [self.ids], [self.out]
+
+
 WORKLOADS = {"gate_up_decode": GateUpDecode, "decode_step": DecodeStep, "prompt_chunk": PromptChunk,
-             "lane_sweep": LaneSweep, "tiny": Tiny}
+             "lane_sweep": LaneSweep, "tiny": Tiny, "embed_rows": EmbedRows}
 
 
 # ----------------------------------------------------------------------------- timing
@@ -495,16 +547,28 @@ class OracleSample:
         self.xb, self.cb = synth.bits_u16(x), codes.numpy()
         self.sb, self.bb = synth.bits_u16(s), synth.bits_u16(b)
         self.threads = host_cores()
+        self.embed = bool(shape.get("embed"))
+        if self.embed:
+            self.threads = 1
+            self.embed_scale = int(synth.bits_u16(torch_bf16_scalar(math.sqrt(self.K)))[0])
 
     def units(self, rows: int) -> float:
+        if self.embed:
+            return rows * (self.K * self.bits // 8 + 4 * self.K // self.group + 4 + 2 * self.K) / 1e9
         if self.unit == "TFLOP/s":
             return 2.0 * self.M * rows * self.K / 1e12
         return (rows * self.K * self.bits // 8 + 4 * rows * self.K // self.group) / 1e9
 
     def run(self, rows: int) -> float:
         t0 = time.perf_counter()
-        self.orc.qmm(self.bits, self.group, self.xb, self.cb[:rows], self.sb[:rows], self.bb[:rows],
-                     nthreads=self.threads)
+        if self.embed:   # rows of the table gathered (one thread: the oracle's gather is not threaded)
+            import numpy as np
+            ids = np.arange(rows, dtype=np.int32)
+            self.orc.embed_rows(self.bits, self.group, self.cb[:rows], self.sb[:rows], self.bb[:rows], ids,
+                                self.embed_scale)
+        else:
+            self.orc.qmm(self.bits, self.group, self.xb, self.cb[:rows], self.sb[:rows], self.bb[:rows],
+                         nthreads=self.threads)
         return time.perf_counter() - t0
 
     def rows_for(self, seconds: float) -> int:
@@ -513,6 +577,9 @@ class OracleSample:
         return int(max(1, min(self.N, n * seconds / dt)))
 
     def describe(self, rows: int, reps: int) -> str:
+        if self.embed:
+            return (f"{reps} x {rows} gathered rows of K={self.K}, {self.bits}-bit g{self.group} times a bf16 "
+                    f"scale; oracle on one thread")
         return (f"{reps} x {rows} of {self.N} output rows of one projection of the workload (M={self.M}, "
                 f"K={self.K}, {self.bits}-bit g{self.group}); float64 oracle threaded over rows")
 
@@ -534,7 +601,13 @@ WORKLOAD_ORACLE_SHAPES = {   # the projection each workload's oracle sample take
                                    K=s.DECODER_LAYER_SHAPES["qkv"][1], seed=s.step_seed(s.PROMPT_CHUNK["seed"], 0, 0)),
     "lane_sweep": lambda s: dict(bits=4, group=64, M=2, N=s.SWEEP_SHAPE["N"], K=s.SWEEP_SHAPE["K"],
                                  seed=s.SWEEP_SHAPE["seed"]),
+    "embed_rows": lambda s: dict(bits=4, group=64, M=1, N=4096, K=s.HEAD_SHAPE[1], seed=s.EMBED_SEED, embed=True),
 }
+
+
+def torch_bf16_scalar(v: float):
+    import torch
+    return torch.tensor([v], dtype=torch.float32).to(torch.bfloat16)
 
 
 def workload_unit(name: str) -> str:

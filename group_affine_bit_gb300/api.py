@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             "affqmm_dequant": (i32, [wp, vp, vp]),
             "affqmm_workspace_status": (i32, [vp, vp]),
             "affqmm_run_noalloc": (i32, [wp, vp, i64, vp, vp]),
+            "affqmm_embed_rows": (i32, [wp, vp, i64, i32, ctypes.c_uint16, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -236,3 +237,22 @@ def run_noalloc(w: PackedWeight, x: torch.Tensor, y: torch.Tensor, stream=None) 
     _check(lib().affqmm_run_noalloc(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), _stream_ptr(stream)),
            "affqmm_run_noalloc")
     return y
+
+
+def embed_rows(w: PackedWeight, ids: torch.Tensor, scale: float | None = None, out: torch.Tensor | None = None,
+               status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[t, k] = bf16(W[ids[t], k] * bf16(scale)) (or W's rows when scale is None),
+    W = bf16(s*q + b): rows gathered from the packed table.  ids: int32 CUDA [T]."""
+    if not ids.is_cuda or ids.dtype != torch.int32 or ids.dim() != 1 or not ids.is_contiguous():
+        raise ValueError("ids must be a contiguous int32 CUDA vector")
+    T = ids.shape[0]
+    if out is None:
+        out = torch.empty(T, w.K, dtype=torch.bfloat16, device=ids.device)
+    if out.dtype != torch.bfloat16 or tuple(out.shape) != (T, w.K) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous bf16 [{T}, {w.K}] tensor")
+    sbits = 0 if scale is None else int(torch.tensor([scale], dtype=torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+    cw = w.cstruct()
+    _check(lib().affqmm_embed_rows(ctypes.byref(cw), ids.data_ptr(), T, 0 if scale is None else 1, sbits,
+                                   out.data_ptr(), status.data_ptr() if status is not None else None,
+                                   _stream_ptr(stream)), "affqmm_embed_rows")
+    return out

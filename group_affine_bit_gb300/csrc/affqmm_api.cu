@@ -392,6 +392,25 @@ int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* stream) {
     return AFFQMM_OK;
 }
 
+int affqmm_embed_rows(const affqmm_weight* w, const int32_t* ids, int64_t T, int has_scale, uint16_t scale,
+                      uint16_t* out, uint32_t* status, void* stream) {
+    int rc = check_weight(w);
+    if (rc) return rc;
+    if (T < 0) return AFFQMM_E_ARG;
+    if (T == 0 || w->K == 0) return AFFQMM_OK;
+    if (!ids || !out) return AFFQMM_E_NULL;
+    if (w->N == 0) return AFFQMM_E_SHAPE;  // no row to gather
+    if (!aligned(out, 16) || !aligned(ids, 4) || (status && !aligned(status, 4))) return AFFQMM_E_ALIGN;
+    if (T > ((int64_t)1 << 31) / ((w->K + KBLK - 1) / KBLK)) return AFFQMM_E_SHAPE;
+    DeviceInfo* d = nullptr;
+    rc = device_info(&d);
+    if (rc) return rc;
+    if (launch_embed(w->bits, w->group, w->packed, w->N, w->K, ids, T, has_scale ? 1 : 0, scale, out, status,
+                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return AFFQMM_E_CUDA;
+    return AFFQMM_OK;
+}
+
 int affqmm_workspace_status(void* workspace, void* stream) {
     if (!workspace) return AFFQMM_E_NULL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

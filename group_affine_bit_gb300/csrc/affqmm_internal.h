@@ -114,5 +114,8 @@ cudaError_t launch_pack(int bits, int group, int64_t N, int64_t K, const uint8_t
                         cudaStream_t st);
 cudaError_t launch_dequant(int bits, int group, int64_t N, int64_t K, const void* packed,
                            uint16_t* out, cudaStream_t st);
+// embed.cu: rows ids[0..T) of the table, optionally times a bf16 scale.
+cudaError_t launch_embed(int bits, int group, const void* packed, int64_t N, int64_t K, const int32_t* ids,
+                         int64_t T, int has_scale, uint16_t scale, uint16_t* out, uint32_t* status, cudaStream_t st);
 
 }  // namespace affqmm

@@ -123,11 +123,17 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* addr, unsigned v)
 
 // A bounded wait that also gives up when another role of the CTA has aborted
 // (then every role leaves its loop and the CTA finishes).
+// A suspended try_wait also returns (false) when another thread arrives on
+// the barrier without completing the phase, so the abort flag and the clock
+// are looked at only every eighth return: those early wake-ups stay cheap.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                               uint32_t* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    for (;;) {
+#pragma unroll 1
+        for (int r = 0; r < 8; ++r)
+            if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitLimitCycles) {
             *abort_flag = 1;
@@ -135,7 +141,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
             return false;
         }
     }
-    return true;
 }
 
 // The same for threads that are not on the critical path (the producers,

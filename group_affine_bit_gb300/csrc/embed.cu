@@ -1,0 +1,104 @@
+// embed.cu -- scaled embedding rows gathered from a packed affine table:
+//
+//     out[t, k] = bf16( W[ids[t], k] * scale ),   W[n, k] = bf16(s * q + b)
+//
+// ("cuda gemma4: images on the 12B" page, the embed_rows commit: MLX affine
+// tables at 2..8 bits, each dequantized bf16 value multiplied by a bf16
+// scale -- Gemma's bf16(sqrt(hidden)) -- and rounded again.)  Both roundings
+// are of exact values: fma.rn.bf16x2 for the weight (affqmm_format.cuh, the
+// arithmetic of the projection kernels) and mul.rn.bf16x2 for the product.
+//
+// One thread per (row t, 128-deep block): it loads the row's codes and
+// scale/bias words of that block from the packed table (the same layout the
+// projections read, so a tied head serves as the embedding table), makes the
+// 128 values and writes them as 16 contiguous 16-byte stores.  Memory-bound:
+// the packed bytes of the gathered rows in, 2 bytes per value out.
+#include <cuda_bf16.h>
+
+#include "affqmm_format.cuh"
+#include "affqmm_internal.h"
+
+namespace affqmm {
+namespace {
+
+constexpr int E_THREADS = 128;
+
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int BITS, int GROUP>
+__global__ void __launch_bounds__(E_THREADS) embed_kernel(const uint8_t* __restrict__ packed, int64_t N, int64_t K,
+                                                          int KB, const int32_t* __restrict__ ids, int64_t T,
+                                                          int has_scale, uint32_t scale2, uint16_t* __restrict__ out,
+                                                          uint32_t* status) {
+    const int64_t item = (int64_t)blockIdx.x * E_THREADS + threadIdx.x;
+    if (item >= T * KB) return;
+    const int64_t t = item / KB;
+    const int kb = (int)(item - t * KB);
+    const int64_t n = ids[t];
+    uint16_t* dst = out + t * K + (int64_t)kb * KBLK;
+    const int64_t kleft = K - (int64_t)kb * KBLK;  // values of this block inside the row (8-aligned, >= 32)
+    uint32_t w[KBLK / 2];
+    if (n < 0 || n >= N) {  // not a row of the table: zeros, and say so
+#pragma unroll
+        for (int c = 0; c < KBLK / 2; ++c) w[c] = 0u;
+        if (status && kb == 0) atomicOr(status, 2u);
+    } else {
+        const uint8_t* blk = packed + ((n / TILE_N) * KB + kb) * (int64_t)block_bytes(BITS, GROUP);
+        const int r = (int)(n % TILE_N);
+        uint32_t cw[4 * BITS];
+        load_row_codes<BITS>(blk, r, cw);
+        uint32_t sbw[sb_words(GROUP)];
+        load_row_sb<GROUP>(blk + sb_offset(BITS, GROUP, r), sbw);
+        weight_pairs<BITS, GROUP, 0, KBLK / 2>(cw, sbw, w);
+        if (has_scale) {
+#pragma unroll
+            for (int c = 0; c < KBLK / 2; ++c) w[c] = bf2_mul(w[c], scale2);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < KBLK / 8; ++c)  // 8 values (16 bytes) per store
+        if (8 * c < kleft) st_v4(dst + 8 * c, w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+template <int BITS>
+cudaError_t embed_bits(int group, const uint8_t* packed, int64_t N, int64_t K, int KB, const int32_t* ids, int64_t T,
+                       int has_scale, uint32_t scale2, uint16_t* out, uint32_t* status, cudaStream_t st) {
+    const int64_t items = T * KB;
+    const unsigned grid = (unsigned)((items + E_THREADS - 1) / E_THREADS);
+    if (group == 32)
+        embed_kernel<BITS, 32><<<grid, E_THREADS, 0, st>>>(packed, N, K, KB, ids, T, has_scale, scale2, out, status);
+    else if (group == 64)
+        embed_kernel<BITS, 64><<<grid, E_THREADS, 0, st>>>(packed, N, K, KB, ids, T, has_scale, scale2, out, status);
+    else
+        embed_kernel<BITS, 128><<<grid, E_THREADS, 0, st>>>(packed, N, K, KB, ids, T, has_scale, scale2, out, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_embed(int bits, int group, const void* packed, int64_t N, int64_t K, const int32_t* ids,
+                         int64_t T, int has_scale, uint16_t scale, uint16_t* out, uint32_t* status, cudaStream_t st) {
+    const int KB = (int)((K + KBLK - 1) / KBLK);
+    if (T == 0 || KB == 0) return cudaSuccess;
+    const uint8_t* src = static_cast<const uint8_t*>(packed);
+    const uint32_t scale2 = (uint32_t)scale * 0x00010001u;  // the scale in both halves
+    switch (bits) {
+        case 2: return embed_bits<2>(group, src, N, K, KB, ids, T, has_scale, scale2, out, status, st);
+        case 3: return embed_bits<3>(group, src, N, K, KB, ids, T, has_scale, scale2, out, status, st);
+        case 4: return embed_bits<4>(group, src, N, K, KB, ids, T, has_scale, scale2, out, status, st);
+        case 5: return embed_bits<5>(group, src, N, K, KB, ids, T, has_scale, scale2, out, status, st);
+        case 6: return embed_bits<6>(group, src, N, K, KB, ids, T, has_scale, scale2, out, status, st);
+        case 8: return embed_bits<8>(group, src, N, K, KB, ids, T, has_scale, scale2, out, status, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace affqmm

@@ -79,6 +79,7 @@ GATE_UP_DECODE = dict(M=1, K=3840, N=30720, bits=4, group=64, seed=1)
 DECODE_STEP_SEED = 2
 PROMPT_CHUNK = dict(M=128, bits=4, group=64, seed=3)
 SWEEP_SHAPE = dict(K=3840, N=15360, seed=4)
+EMBED_SEED = 5
 SWEEP_CASES = [(2, 4, 64), (4, 4, 64), (8, 4, 64), (16, 4, 64),
                (16, 8, 32), (16, 3, 64), (16, 2, 128)]   # (M, bits, group)
 

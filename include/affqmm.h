@@ -151,6 +151,23 @@ AFFQMM_API int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint
  * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_CUDA. */
 AFFQMM_API int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* stream);
 
+/* Scaled embedding rows gathered from a packed table: for t < T,
+ *     out[t, k] = bf16( W[ids[t], k] * scale ),  W[n, k] = bf16(s * q + b),
+ * each of the two roundings applied to an exact value ("cuda gemma4: images
+ * on the 12B" page, the embed_rows commit: Gemma's embedding times
+ * bf16(sqrt(hidden))).  The table is any packed weight (a tied head serves).
+ *   w          host pointer to the weight view: N rows (vocabulary), K values each
+ *   ids        device, int32 [T]
+ *   T          rows to gather; 0 launches nothing
+ *   has_scale  0: out = W's rows (no second rounding); else multiply by `scale`
+ *   scale      bf16 bit pattern
+ *   out        device, bf16 [T, K] row-major, 16-byte aligned; fully written
+ *   status     device uint32 or NULL: an id outside [0, N) gives a zero row and
+ *              sets bit 1 of *status (the caller zeroes it beforehand)
+ * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_ARG (T < 0), E_CUDA. */
+AFFQMM_API int affqmm_embed_rows(const affqmm_weight* w, const int32_t* ids, int64_t T, int has_scale,
+                                 uint16_t scale, uint16_t* out, uint32_t* status, void* stream);
+
 /* Read and clear the device status word of a workspace (synchronizes
  * `stream`).  Returns AFFQMM_OK, or AFFQMM_E_TIMEOUT when a kernel that used
  * this workspace gave up a bounded wait (its outputs are then invalid). */

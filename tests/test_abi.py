@@ -120,3 +120,16 @@ def test_pack_and_dequant_refusals(L):
     assert names[L.affqmm_dequant(ctypes.byref(w), None, None)] == "AFFQMM_E_NULL"
     assert names[L.affqmm_dequant(ctypes.byref(w), 0x300001, None)] == "AFFQMM_E_ALIGN"
     assert names[L.affqmm_workspace_status(None, None)] == "AFFQMM_E_NULL"
+
+
+def test_embed_rows_refusals_before_any_launch(L):
+    w = _w()
+    rc = L.affqmm_embed_rows(ctypes.byref(w), 0x200000, -1, 1, 0x4000, 0x300000, None, None)
+    assert api.STATUS_NAMES[rc] == "AFFQMM_E_ARG"
+    bad = _w(bits=7)
+    rc = L.affqmm_embed_rows(ctypes.byref(bad), 0x200000, 4, 1, 0x4000, 0x300000, None, None)
+    assert api.STATUS_NAMES[rc] == "AFFQMM_E_BITS"
+    rc = L.affqmm_embed_rows(ctypes.byref(w), None, 4, 1, 0x4000, 0x300000, None, None)
+    assert api.STATUS_NAMES[rc] == "AFFQMM_E_NULL"
+    rc = L.affqmm_embed_rows(ctypes.byref(w), 0x200000, 4, 1, 0x4000, 0x300008, None, None)
+    assert api.STATUS_NAMES[rc] == "AFFQMM_E_ALIGN"
