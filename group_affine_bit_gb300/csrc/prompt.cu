@@ -344,13 +344,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 }
 
 // The tiles that several runs share: y = the runs' fp32 partials added in run
-// order.  Grid: (every tile of every projection, 16-row blocks of the
-// activation rows); thread = one of the tile's 256 weight rows.  Tiles that
-// one run owned were stored by prompt_kernel and are skipped.
-__global__ void __launch_bounds__(P_TILE_N) prompt_merge_kernel(const __grid_constant__ PromptParams p) {
+// order.  Grid: (4-row blocks of the activation rows, every tile of every
+// projection); a thread owns four consecutive weight rows n of one activation
+// row m (a 16-byte load from each run's partial: a warp reads 512 contiguous
+// bytes), so the whole merge is a few rounds of fully parallel L2 reads.
+// Tiles that one run owned were stored by prompt_kernel and are skipped.
+constexpr int P_MERGE_THREADS = 256;
+__global__ void __launch_bounds__(P_MERGE_THREADS) prompt_merge_kernel(const __grid_constant__ PromptParams p) {
     pdl_launch_dependents();  // the next kernel's prologue and weight copies may start
     pdl_wait();               // the partials of prompt_kernel are complete and visible
-    const int t_all = (int)blockIdx.x;
+    const int t_all = (int)blockIdx.y;
     int pi = 0;
     for (int i = 1; i < p.nproj; ++i)
         if (t_all >= p.proj[i].ctr_begin) pi = i;
@@ -360,24 +363,27 @@ __global__ void __launch_bounds__(P_TILE_N) prompt_merge_kernel(const __grid_con
     const int t0 = tile * KB, t1 = t0 + KB - 1;
     const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
     if (cf == cl) return;
-    const int nt = (int)threadIdx.x;
-    const int64_t n = (int64_t)tile * P_TILE_N + nt;
-    const int m0 = 16 * (int)blockIdx.y;
-    if (n >= P.N || m0 >= p.M) return;
-    float acc[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    const int m = 4 * (int)blockIdx.x + ((int)threadIdx.x >> 6);
+    const int n4 = 4 * ((int)threadIdx.x & 63);  // weight row within the 256-row tile
+    const int64_t n = (int64_t)tile * P_TILE_N + n4;
+    if (m >= p.M || n >= P.N) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int cb = cf; cb <= cl; ++cb) {
         const int b0 = (int)((int64_t)cb * U / PC);
         const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
-        const float* src = p.slots + (size_t)sc * kPromptSlotFloats + (size_t)m0 * P_TILE_N + nt;
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            if (m0 + e < p.M) acc[e] += __ldcg(src + (size_t)e * P_TILE_N);
+        const float4 f = __ldcg(
+            reinterpret_cast<const float4*>(p.slots + (size_t)sc * kPromptSlotFloats + (size_t)m * P_TILE_N + n4));
+        acc.x += f.x;
+        acc.y += f.y;
+        acc.z += f.z;
+        acc.w += f.w;
     }
+    uint16_t* yr = P.y + (int64_t)m * P.N + n;
+    const float av[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-        if (m0 + e < p.M) P.y[(int64_t)(m0 + e) * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
+    for (int e = 0; e < 4; ++e)
+        if (n + e < P.N) yr[e] = __bfloat16_as_ushort(__float2bfloat16_rn(av[e]));
 }
 
 template <int BITS, int GROUP>
@@ -390,8 +396,8 @@ cudaError_t launch_prompt_bg(const PromptParams& p, const CUtensorMap& map, int 
     cudaError_t e = launch_pdl(prompt_kernel<BITS, GROUP>, grid, P_THREADS, prompt_smem_for<BITS, GROUP>(), st, p, map);
     if (e != cudaSuccess) return e;
     const PromptProj& last = p.proj[p.nproj - 1];
-    const dim3 mgrid((unsigned)(last.ctr_begin + last.tiles), (unsigned)((p.M + 15) / 16));
-    return launch_pdl(prompt_merge_kernel, mgrid, P_TILE_N, 0, st, p);
+    const dim3 mgrid((unsigned)((p.M + 3) / 4), (unsigned)(last.ctr_begin + last.tiles));
+    return launch_pdl(prompt_merge_kernel, mgrid, P_MERGE_THREADS, 0, st, p);
 }
 
 template <int BITS>
