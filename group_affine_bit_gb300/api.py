@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 import torch
 
@@ -99,9 +99,15 @@ class PackedWeight:
     N: int
     K: int
     packed: torch.Tensor
+    _c: CWeight | None = field(default=None, repr=False, compare=False)
+    _ws: dict = field(default_factory=dict, repr=False, compare=False)   # (M, device) -> workspace bytes
 
     def cstruct(self) -> CWeight:
-        return CWeight(self.bits, self.group, self.N, self.K, self.packed.data_ptr() if self.packed.numel() else None)
+        """The C view of this weight (built once: the storage never moves)."""
+        if self._c is None:
+            self._c = CWeight(self.bits, self.group, self.N, self.K,
+                              self.packed.data_ptr() if self.packed.numel() else None)
+        return self._c
 
 
 def packed_bytes(bits: int, group: int, N: int, K: int) -> int:
@@ -127,10 +133,14 @@ def pack(codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, bits: 
 
 
 def workspace_bytes(w: PackedWeight, M: int) -> int:
-    out = ctypes.c_size_t(0)
-    cw = w.cstruct()
-    _check(lib().affqmm_workspace_bytes(ctypes.byref(cw), M, ctypes.byref(out)), "affqmm_workspace_bytes")
-    return out.value
+    key = (M, torch.cuda.current_device())
+    got = w._ws.get(key)
+    if got is None:
+        out = ctypes.c_size_t(0)
+        cw = w.cstruct()
+        _check(lib().affqmm_workspace_bytes(ctypes.byref(cw), M, ctypes.byref(out)), "affqmm_workspace_bytes")
+        got = w._ws[key] = out.value
+    return got
 
 
 def _warray(ws):
