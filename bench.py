@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 METRIC = "affine-4bit qmm packed-weight GB/s vs HBM peak (M=1..16); TFLOP/s at M=128"
 L2_BYTES = 129 * 10 ** 6
 KERNEL_SOURCES = ["group_affine_bit_gb300/csrc/decode.cu", "group_affine_bit_gb300/csrc/prompt.cu",
+                  "group_affine_bit_gb300/csrc/embed.cu",
                   "group_affine_bit_gb300/csrc/affqmm_format.cuh", "group_affine_bit_gb300/csrc/affqmm_tc.cuh",
                   "group_affine_bit_gb300/csrc/affqmm_async.cuh"]
 
@@ -227,7 +228,13 @@ class Case:
 
     @property
     def launches(self) -> int:
+        """Launches of the dominant kernel (decode or prompt kernel)."""
         return 1 if self.M <= 16 else -(-self.M // 128)
+
+    @property
+    def kernels(self) -> int:
+        """All of the library's kernel launches: a prompt chunk also launches its merge kernel."""
+        return 1 if self.M <= 16 else 2 * (-(-self.M // 128))
 
     def oracle_shape(self):
         return dict(bits=self.bits, group=self.group, M=self.M, N=self.N, K=self.K, seed=self.seed)
@@ -254,6 +261,10 @@ class Workload:
     @property
     def launches_per_step(self) -> int:
         return sum(c.launches for c in self.cases)
+
+    @property
+    def kernels_per_step(self) -> int:
+        return sum(c.kernels for c in self.cases)
 
     @property
     def units_per_step(self) -> float:
@@ -414,6 +425,7 @@ class EmbedRows(Workload):
         self.api.embed_rows(self.w, self.ids, math.sqrt(5376.0), out=self.out)
 
     launches_per_step = 1
+    kernels_per_step = 1
 
     @property
     def packed_row_bytes(self) -> int:
@@ -717,7 +729,7 @@ def main(argv=None):
                 "warmup": warmup, "ms_per_step": t_max / steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": wl.config(), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clocks, "kernel_src_digest": source_digest()}
+                "gpu_launches": steps * wl.kernels_per_step, "clocks": clocks, "kernel_src_digest": source_digest()}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
