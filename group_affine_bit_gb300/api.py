@@ -85,8 +85,13 @@ def _check(rc: int, what: str):
         raise AffqmmError(rc, what)
 
 
-def _stream_ptr(stream) -> int:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)   # cheap current-stream lookup, when present
+
+
+def _stream_ptr(stream, device_index: int | None = None) -> int:
     if stream is None:
+        if _raw_stream is not None:
+            return int(_raw_stream(torch.cuda.current_device() if device_index is None else device_index))
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream)
 
@@ -175,11 +180,16 @@ class Workspace:
 _workspaces: dict = {}
 
 
-def default_workspace(device) -> Workspace:
-    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
-    if key not in _workspaces:
-        _workspaces[key] = Workspace(device)
-    return _workspaces[key]
+def default_workspace(device, stream_ptr: int | None = None) -> Workspace:
+    """One workspace per (device, stream): calls on one stream never overlap."""
+    index = torch.device(device).index if not isinstance(device, int) else device
+    if stream_ptr is None:
+        stream_ptr = _stream_ptr(None, index)
+    key = (index, stream_ptr)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = _workspaces[key] = Workspace(torch.device("cuda", index))
+    return ws
 
 
 def _check_x(x: torch.Tensor, K: int):
@@ -192,14 +202,16 @@ def run(w: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, workspa
     """y[M, N] = bf16(x @ dequant(W)^T) with fp32 accumulation."""
     _check_x(x, w.K)
     M = x.shape[0]
+    dev = x.get_device()
     if y is None:
         y = torch.empty(M, w.N, dtype=torch.bfloat16, device=x.device)
-    ws = workspace or default_workspace(x.device)
+    sp = _stream_ptr(stream, dev)
+    ws = workspace or default_workspace(dev, sp)
     need = workspace_bytes(w, M)
     buf = ws.get(need)
     cw = w.cstruct()
     _check(lib().affqmm_run(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), buf.data_ptr() if need else None,
-                            buf.numel(), _stream_ptr(stream)), "affqmm_run")
+                            buf.numel(), sp), "affqmm_run")
     return y
 
 
@@ -210,13 +222,14 @@ def run_stacked(ws_list, x: torch.Tensor, ys=None, workspace: Workspace | None =
     M = x.shape[0]
     if ys is None:
         ys = [torch.empty(M, w.N, dtype=torch.bfloat16, device=x.device) for w in ws_list]
-    wsp = workspace or default_workspace(x.device)
+    sp = _stream_ptr(stream, x.get_device())
+    wsp = workspace or default_workspace(x.get_device(), sp)
     need = workspace_bytes_stacked(ws_list, M)
     buf = wsp.get(need)
     arr = _warray(ws_list)
     yp = (ctypes.c_void_p * len(ys))(*[y.data_ptr() for y in ys])
     _check(lib().affqmm_run_stacked(len(ws_list), arr, x.data_ptr(), M, yp, buf.data_ptr() if need else None,
-                                    buf.numel(), _stream_ptr(stream)), "affqmm_run_stacked")
+                                    buf.numel(), sp), "affqmm_run_stacked")
     return ys
 
 
