@@ -249,7 +249,7 @@ def workspace_status(buf: torch.Tensor, stream=None) -> int:
 def run_noalloc(w: PackedWeight, x: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Tensor:
     """affqmm_run_noalloc: y = bf16(x @ dequant(W)^T) for M <= 16 rows, with no
     workspace.  For callers that cannot allocate device memory; the library
-    works in its own fixed 3 MiB scratch array instead, shared by every call on
+    works in its own fixed 8 MiB scratch array instead, shared by every call on
     the device, so calls must not overlap on the GPU.  `y` must be given: this
     wrapper allocates nothing either."""
     _check_x(x, w.K)

@@ -26,16 +26,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // that changes what a call computes on a given device).
 struct DeviceInfo {
     int sms = 0;
+    int dec_ctas_per_sm = 0;  // decode CTAs resident per SM
     bool ok = false;
     bool is_sm103 = false;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_once[kMaxDevices];
-
-// Decode kernel shape: one CTA per SM -- it holds all 512 tensor-memory
-// columns -- with a ring of up to 12 stages (weight block and activation
-// tile), 100-150 KB of weights in flight per SM.
-constexpr int kDecCtasPerSm = 1;
 
 int device_info(DeviceInfo** out) {
     int dev = 0;
@@ -48,7 +44,7 @@ int device_info(DeviceInfo** out) {
         d.sms = prop.multiProcessorCount;
         d.is_sm103 = prop.major == 10 && prop.minor == 3;
         if (!d.is_sm103) { d.ok = true; return; }
-        if (decode_allow_smem() != cudaSuccess) return;
+        if (decode_allow_smem(&d.dec_ctas_per_sm) != cudaSuccess) return;
         if (prompt_allow_smem() != cudaSuccess) return;
         d.ok = true;
     });
@@ -94,7 +90,7 @@ int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, De
     p.KB = KB;
     p.K = K;
     p.M = (int32_t)M;
-    const int64_t resident = (int64_t)d.sms * kDecCtasPerSm;
+    const int64_t resident = (int64_t)d.sms * d.dec_ctas_per_sm;
     int64_t ctas = 0, tiles_total = 0;
     for (int i = 0; i < count; ++i) {
         DecProj& P = p.proj[i];
@@ -110,7 +106,7 @@ int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, De
         ctas += P.nctas;
         tiles_total += tiles;
     }
-    if (4 * tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
+    if (kDecCountersPerTile * tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
     plan->grid = (int)ctas;
     plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kDecSlotFloats * sizeof(float) : 0;
     return AFFQMM_OK;
@@ -148,9 +144,9 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// x [M, K] bf16 row-major as 64 (k) x `box_rows` boxes (the decode kernel
-// loads M rows, the prompt kernel 128) with the 128-byte
-// swizzle the tensor core reads; rows past M and k past K read as zero.
+// x [M, K] bf16 row-major as 64 (k) x 128-row boxes with the 128-byte
+// swizzle the tensor core reads (the prompt kernel); rows past M and k past
+// K read as zero.
 int make_x_map(const uint16_t* x, int64_t M, int64_t K, int box_rows, CUtensorMap* map) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return AFFQMM_E_CUDA;
@@ -160,6 +156,22 @@ int make_x_map(const uint16_t* x, int64_t M, int64_t K, int box_rows, CUtensorMa
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? AFFQMM_OK : AFFQMM_E_CUDA;
+}
+
+// x [M, K] bf16 for the decode kernel: boxes of 136 k x M rows, unswizzled,
+// so a block's tile lands as M rows of 272 bytes (its 128 k and 8 of the next
+// block, which the kernel does not use); k past K reads as zero.
+int make_x_map_decode(const uint16_t* x, int64_t M, int64_t K, CUtensorMap* map) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return AFFQMM_E_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {136, (cuuint32_t)M};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? AFFQMM_OK : AFFQMM_E_CUDA;
 }
@@ -279,7 +291,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         bind_workspace(&plan, workspace);
         for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i];
         CUtensorMap map;
-        rc = make_x_map(x, M, K, (int)M, &map);
+        rc = make_x_map_decode(x, M, K, &map);
         if (rc) return rc;
         if (launch_decode(ws[0].bits, ws[0].group, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
         return AFFQMM_OK;
@@ -322,7 +334,7 @@ const char* affqmm_strerror(int status) {
         case AFFQMM_E_ARG: return "bad argument (count or mismatched stacked weights)";
         case AFFQMM_E_DEVICE: return "the current device is not an sm_103 GPU";
         case AFFQMM_E_SCRATCH:
-            return "affqmm_run_noalloc: M > 16, or the work needs more than its 3 MiB built-in scratch";
+            return "affqmm_run_noalloc: M > 16, or the work needs more than its 8 MiB built-in scratch";
         default: return "unknown affqmm status";
     }
 }
@@ -494,15 +506,15 @@ extern "C" int affqmm_run_noalloc(const affqmm_weight* w, const uint16_t* x, int
     void* scratch = nullptr;
     rc = noalloc_scratch(&scratch);
     if (rc) return rc;
-    // The status word and this call's merge counters (four per 128-row tile)
+    // The status word and this call's merge counters (eight per 128-row tile)
     // must start at zero; whatever an earlier call left in them is cleared on
     // the stream, ahead of the kernel.  The partial-sum slots need no clearing.
-    const size_t zeroed = kStatusBytes + (size_t)4 * (size_t)plan.p.proj[0].tiles * sizeof(uint32_t);
+    const size_t zeroed = kStatusBytes + (size_t)kDecCountersPerTile * (size_t)plan.p.proj[0].tiles * sizeof(uint32_t);
     if (cudaMemsetAsync(scratch, 0, zeroed, st) != cudaSuccess) return AFFQMM_E_CUDA;
     bind_workspace(&plan, scratch);
     plan.p.proj[0].y = y;
     CUtensorMap map;
-    rc = make_x_map(x, M, w->K, (int)M, &map);
+    rc = make_x_map_decode(x, M, w->K, &map);
     if (rc) return rc;
     if (launch_decode(w->bits, w->group, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
     return AFFQMM_OK;

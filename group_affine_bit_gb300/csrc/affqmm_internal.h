@@ -25,7 +25,7 @@ struct DecProj {
     int32_t units;        // tiles * k-blocks
     int32_t nctas;        // CTAs working on this projection (<= units)
     int32_t cta_begin;    // first CTA of this projection in the grid
-    int32_t ctr_begin;    // first tile of this projection's merge counters (four per tile)
+    int32_t ctr_begin;    // first tile of this projection's merge counters (eight per tile)
     int32_t slot_begin;   // first partial slot (two per CTA)
 };
 
@@ -41,6 +41,7 @@ struct DecParams {
 };
 
 constexpr size_t kDecSlotFloats = 128 * 16;
+constexpr int kDecCountersPerTile = 8;   // one per 16-row group of a tile
 
 // Workspace layout shared by every kernel: a status word, then a fixed region
 // of merge counters (zero between calls: the last user of a counter resets
@@ -103,8 +104,10 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, int threads, size_t
 }
 
 // Launchers (decode.cu, prompt.cu, pack.cu).  They return the launch's error.
-// decode.cu: the tensor map describes x [M, K] bf16 with a 64 x M box.
-cudaError_t decode_allow_smem();
+// decode.cu: the tensor map describes x [M, K] bf16 with a 136 x M box, no
+// swizzle.  decode_allow_smem sets the kernels' shared-memory attributes and
+// reports how many decode CTAs one SM holds.
+cudaError_t decode_allow_smem(int* ctas_per_sm);
 cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st);
 // prompt.cu: the tensor map describes x [M, K] bf16 with a 64 x 128 box.
 cudaError_t prompt_allow_smem();

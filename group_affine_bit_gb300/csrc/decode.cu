@@ -1,41 +1,41 @@
-// decode.cu -- the memory-bound projection for M = 1..16 activation rows, on
-// the 5th-generation tensor cores.
+// decode.cu -- the memory-bound projection for M = 1..16 activation rows.
 //
-// Each 128-row x 128-deep weight block is one tcgen05.mma problem:
-// D[128 weight rows, 16 activation rows] += W (tensor memory) * x^T (shared
-// memory), fp32 in tensor memory.  Per CTA:
-//   * two producer threads stream the blocks (9 KB for 4-bit codes and bf16
-//     scale/bias words) two at a time with 1-D bulk copies into a ring of
-//     weight slots, and a third loads each block's M x 128 activation rows
-//     (TMA, 128-byte swizzle) into a ring of 16-row tiles whose other rows
-//     stay zero;
-//   * four lanes of work take blocks i = 0, 1, 2, 3 (mod 4) of the run; each
-//     has a group of four dequantization warps -- one thread per weight row
-//     reads the row's codes back, rounds every weight once as
-//     bf16(fma(s, q, b)) (affqmm_format.cuh) and stores the row into the
-//     lane's tensor-memory buffer with tcgen05.st, so the A operand never
-//     touches shared memory -- and an MMA warp that issues the block's MMAs
-//     (M = 128, N = 16, K = 16) into the lane's accumulator chain and
-//     commits (at N = 16 a single issuing thread cannot keep up);
-//   * the group that dequantized a tile segment's last block adds the four
-//     chains with tcgen05.ld and stores bf16 y (coalesced along n).
-// One CTA per SM owns all 512 tensor-memory columns.  Every barrier has one
-// owner per phase sequence (stage s always belongs to lane s mod 4), so no
-// parity wait can be satisfied by a phase one round too old.
-// Prior art: the "reg variant" lane projection of the "Gemma 4 12B on the
-// native Metal engine" page (4-bit groups in tensor-op registers, K split per
-// shape); unlike it, every weight is rounded to bf16 before the contraction,
-// as that page's prompt GEMM does.
+// y[m, n] = bf16( sum_k x[m, k] * bf16(s * q[n, k] + b) ), fp32 sums.
 //
-// Work split: the projection's blocks, numbered tile-major, are cut into one
-// contiguous run per resident CTA ("stream-K").  A tile cut by run boundaries
-// gets one fp32 partial per run (its accumulator chains added first, in chain
-// order); the last CTA to arrive (an atomic counter per
-// tile and 32-row quarter, no waiting) adds them in run order and resets the
+// At M <= 16 the work is a stream of packed weights: every byte is read once
+// and the dequantization arithmetic (three bf16x2 operations per two weights)
+// is what the SMs must keep up with.  The dot products go through the warp-
+// level matrix instruction (mma.sync m16n8k16, bf16 in, fp32 accumulate) with
+// the weights as the A fragment straight from the registers that rounded
+// them, so nothing is written back to shared or tensor memory and no warp
+// waits on another warp's arithmetic: one instruction does the 256
+// multiply-adds of 16 rows x 16 k for up to 8 activation rows, where fp32
+// FMAs on the CUDA cores would cost one instruction per weight and row.
+//
+// Per CTA (two per SM):
+//   * one producer thread streams the run's blocks (9 KB at 4 bits, group
+//     64) two at a time with 1-D bulk copies into a ring of weight slots, and
+//     another loads each block's activation tile -- M rows x 136 k, 272 bytes
+//     a row so that the eight rows of a matrix load sit on distinct banks --
+//     with TMA into a ring of tiles whose rows M..15 stay zero;
+//   * eight consumer warps each own 16 rows of every block: thread t (group
+//     g = t/4, class c = t mod 4) reads class c's code words of rows g and
+//     g + 8 and the rows' scale/bias words (affqmm_format.cuh), releases the
+//     slot, loads the activation fragments with ldmatrix, and for each of the
+//     8 16-deep steps rounds four weight pairs -- bf16(fma(s, q, b)), one
+//     rounding -- and issues one mma (two when M > 8) into fp32 registers.
+// Work split ("stream-K"): the projection's blocks, numbered tile-major, are
+// cut into one contiguous run per CTA.  A tile cut by run boundaries gets one
+// fp32 partial per run; the last warp to arrive (an atomic counter per tile
+// and 16-row group, no waiting) adds them in run order and resets the
 // counter.  The cut depends only on the projection, M and the device, so the
-// same inputs give the same bits on every call, alone or stacked.  Every wait
-// is on an mbarrier with a bound; a wait that gives up sets the workspace
-// status word and an abort flag, and every role of the CTA finishes.
+// same inputs give the same bits on every call, alone or stacked.  Every
+// wait is on an mbarrier with a bound; a wait that gives up sets the
+// workspace status word and an abort flag, and every role finishes.
+// Prior art: the "reg variant" lane projection of the "Gemma 4 12B on the
+// native Metal engine" page (4-bit groups held in registers for the
+// matrix-op, K split per shape); unlike it, every weight is rounded to bf16
+// before the contraction, as that page's prompt GEMM does.
 #include <cuda_bf16.h>
 
 #include <cstddef>
@@ -49,76 +49,163 @@
 namespace affqmm {
 namespace {
 
-constexpr int D_LANES = 4;            // (dequant group, MMA issuer, A buffer, chain) lanes of work
-constexpr int D_ISSUER0 = 1;                       // warp 0: weights producer of the even blocks
-constexpr int D_DEQ_WARP0 = 1 + D_LANES;           // then 4 issuers, 4 groups of 4 dequant warps
-constexpr int D_WPROD1 = D_DEQ_WARP0 + 4 * D_LANES; // weights producer of the odd blocks
-constexpr int D_XPROD = D_WPROD1 + 1;              // activations producer
-constexpr int D_THREADS = (D_XPROD + 1) * 32;
-constexpr int D_MMA_N = 16;           // activation rows per MMA (M <= 16)
-constexpr uint32_t D_X_PANEL = D_MMA_N * 128;      // 16 rows x 64 k bf16, 2 KB
-constexpr uint32_t D_X_BYTES = 2 * D_X_PANEL;      // one 128-deep block of x
-constexpr uint32_t D_TMEM_COLS = 512;
-constexpr int D_A_HALVES = 3;                      // A buffers per lane, each half a block deep
-constexpr uint32_t D_A_HALF_COLS = KBLK / 4;        // 32 columns: 64 bf16 per row
-constexpr uint32_t D_A_COLS = D_A_HALVES * D_A_HALF_COLS;  // 96 columns per lane
-constexpr uint32_t D_ACC_COL0 = D_LANES * D_A_COLS;
-// Accumulators: one chain per lane of work (its blocks of the segment), and
-// two segments' worth so the next segment starts while the last one is
-// drained: column D_ACC_COL0 + 16 * (D_LANES * segment buffer + chain).
-constexpr uint32_t D_IDESC = idesc_bf16_f32(128, D_MMA_N);
-// Two rings: activation blocks (held until the block's MMAs are done) and
-// packed weight blocks (held only until the dequantization warps have the
-// codes in registers, so the weight ring covers the HBM latency).  Both
-// depths are multiples of the lanes: slot s always belongs to lane s mod 4,
-// so no barrier is waited on by two threads that could be a phase apart.
-constexpr int D_XRING = 16;
-constexpr int D_WRING_MAX = 24;
-constexpr uint32_t kDecRingBudget = 210u * 1024u;
+constexpr int D_CWARPS = 8;                   // consumer warp w owns rows 16w .. 16w + 15 of every block
+constexpr int D_WPROD = D_CWARPS;             // weights producer warp
+constexpr int D_XPROD = D_CWARPS + 1;         // activations producer warp
+constexpr int D_THREADS = (D_CWARPS + 2) * 32;
+constexpr int D_CTAS_PER_SM = 2;
+constexpr uint32_t D_XROW = 272;              // bytes per activation row of a tile (128 k + 8 of padding)
+constexpr int D_SLOTS_MAX = 16;
+constexpr uint32_t D_SMEM = 110u * 1024u;     // dynamic shared memory per CTA
+constexpr uint32_t D_RING0 = 1024u;           // the ring starts here; the barriers sit below
 
+// A ring slot holds two consecutive blocks of the run (contiguous in memory:
+// one bulk copy) and their two activation tiles.  Its full barrier waits for
+// both producers' bytes; its empty barrier for every consumer warp.
 struct DecSmem {
-    uint64_t wfull[D_WRING_MAX];
-    uint64_t wempty[D_WRING_MAX];
-    uint64_t xfull[D_XRING];
-    uint64_t xempty[D_XRING];
-    uint64_t a_full[D_A_HALVES * D_LANES];   // (lane, A buffer)
-    uint64_t a_empty[D_A_HALVES * D_LANES];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
-    uint32_t tmem_base;
+    uint64_t full[D_SLOTS_MAX];
+    uint64_t empty[D_SLOTS_MAX];
     int abort_flag;
 };
+static_assert(sizeof(DecSmem) <= D_RING0, "barriers fit below the ring");
+
+template <int NB>
+constexpr uint32_t x_tile_bytes() { return 8u * NB * D_XROW; }  // 8 rows per activation block of the mma
+template <int BITS, int GROUP, int NB>
+constexpr uint32_t slot_bytes() { return 2u * (uint32_t)block_bytes(BITS, GROUP) + 2u * x_tile_bytes<NB>(); }
+template <int BITS, int GROUP, int NB>
+constexpr int ring_slots() {
+    return (int)((D_SMEM - 128u - D_RING0) / slot_bytes<BITS, GROUP, NB>()) > D_SLOTS_MAX
+               ? D_SLOTS_MAX
+               : (int)((D_SMEM - 128u - D_RING0) / slot_bytes<BITS, GROUP, NB>());
+}
 
 __device__ __forceinline__ void sts_zero16(uint32_t a) {
     asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
 }
-
-constexpr int dec_wring_for(int block) {
-    return (int)((kDecRingBudget - D_XRING * D_X_BYTES) / (uint32_t)block) / D_LANES * D_LANES > D_WRING_MAX
-               ? D_WRING_MAX
-               : (int)((kDecRingBudget - D_XRING * D_X_BYTES) / (uint32_t)block) / D_LANES * D_LANES;
+__device__ __forceinline__ void ldmatrix_x4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(a)
+                 : "memory");
 }
-template <int BITS, int GROUP>
-constexpr int dec_wring() {
-    return dec_wring_for(block_bytes(BITS, GROUP));
+// d (+)= a (16 x 16 bf16, row) * b (16 x 8 bf16, col), fp32
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// The 16-deep step S of a block: weight pairs 2S and 2S + 1 of the thread's
+// class for its two rows (the A fragment: row g k-low, row g + 8 k-low, row g
+// k-high, row g + 8 k-high) times the activation fragments.
+template <int BITS, int GROUP, int NB, int S>
+__device__ __forceinline__ void mma_step(const uint32_t* wl, const uint32_t* wh, const uint32_t* sl,
+                                         const uint32_t* sh, const uint32_t (&b)[NB][8][2], float* acc) {
+    const uint32_t a0 = class_weight_pair<BITS, GROUP, 2 * S>(wl, sl);
+    const uint32_t a1 = class_weight_pair<BITS, GROUP, 2 * S>(wh, sh);
+    const uint32_t a2 = class_weight_pair<BITS, GROUP, 2 * S + 1>(wl, sl);
+    const uint32_t a3 = class_weight_pair<BITS, GROUP, 2 * S + 1>(wh, sh);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) mma_bf16(acc + 4 * nb, a0, a1, a2, a3, b[nb][S][0], b[nb][S][1]);
+}
+template <int BITS, int GROUP, int NB, int S = 0>
+__device__ __forceinline__ void mma_steps(const uint32_t* wl, const uint32_t* wh, const uint32_t* sl,
+                                          const uint32_t* sh, const uint32_t (&b)[NB][8][2], float* acc) {
+    if constexpr (S < 8) {
+        mma_step<BITS, GROUP, NB, S>(wl, wh, sl, sh, b, acc);
+        mma_steps<BITS, GROUP, NB, S + 1>(wl, wh, sl, sh, b, acc);
+    }
+}
+// The activation fragments of one block: 8 steps x (k low, k high) for each
+// 8-row activation block.  xa is this lane's ldmatrix row address in the tile.
+template <int NB>
+__device__ __forceinline__ void load_x_frags(uint32_t xa, uint32_t (&b)[NB][8][2]) {
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            ldmatrix_x4(xa + 8u * D_XROW * nb + 64u * q, b[nb][2 * q][0], b[nb][2 * q][1], b[nb][2 * q + 1][0],
+                        b[nb][2 * q + 1][1]);
 }
 
-template <int BITS, int GROUP>
-__global__ void __launch_bounds__(D_THREADS, 1)
+// End of a tile segment (the run's last block of a tile, or of the run): store
+// y, or publish this run's partial and, if it is the last to arrive, add all
+// runs' partials in run order.  acc[4 nb + e]: weight row (e < 2 ? lo : hi),
+// activation row 8 nb + 2c + (e & 1).
+template <int NB>
+__device__ __forceinline__ void segment_end(const DecParams& p, const DecProj& P, float* acc, int tile, bool whole,
+                                            bool first_seg, int cta, int U, int PC, int KB, int M, int warp,
+                                            int lane, int r_lo, int c) {
+    const int r_hi = r_lo + 8;
+    const int64_t n_lo = (int64_t)tile * TILE_N + r_lo;
+    if (whole) {
+#pragma unroll
+        for (int e = 0; e < 4 * NB; ++e) {
+            const int m = 8 * (e >> 2) + 2 * c + (e & 1);
+            const int64_t n = n_lo + ((e & 2) ? 8 : 0);
+            if (m < M && n < P.N) P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
+        }
+        return;
+    }
+    const int slot = P.slot_begin + 2 * cta + (first_seg ? 0 : 1);
+    float* sp = p.partials + (size_t)slot * kDecSlotFloats;
+#pragma unroll
+    for (int e = 0; e < 4 * NB; ++e) {
+        const int m = 8 * (e >> 2) + 2 * c + (e & 1);
+        const int r = (e & 2) ? r_hi : r_lo;
+        if (m < M) __stcg(sp + r * 16 + m, acc[e]);
+    }
+    __syncwarp();
+    unsigned prev = 0;
+    unsigned* ctr = &p.counters[(size_t)(P.ctr_begin + tile) * D_CWARPS + warp];
+    if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    __syncwarp();
+    const int t0 = tile * KB, t1 = t0 + KB - 1;
+    const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
+    if (prev != (unsigned)(cl - cf)) return;
+    float sum[4 * NB];
+#pragma unroll
+    for (int e = 0; e < 4 * NB; ++e) sum[e] = 0.f;
+    for (int cb = cf; cb <= cl; ++cb) {
+        const int b0 = (int)((int64_t)cb * U / PC);
+        const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
+        const float* q = p.partials + (size_t)sc * kDecSlotFloats;
+#pragma unroll
+        for (int e = 0; e < 4 * NB; ++e) {
+            const int m = 8 * (e >> 2) + 2 * c + (e & 1);
+            const int r = (e & 2) ? r_hi : r_lo;
+            if (m < M) sum[e] += __ldcg(q + r * 16 + m);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4 * NB; ++e) {
+        const int m = 8 * (e >> 2) + 2 * c + (e & 1);
+        const int64_t n = n_lo + ((e & 2) ? 8 : 0);
+        if (m < M && n < P.N) P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum[e]));
+    }
+    __syncwarp();
+    if (lane == 0) *ctr = 0u;
+}
+
+template <int BITS, int GROUP, int NB>
+__global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
     decode_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap xmap) {
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     constexpr int BB = block_bytes(BITS, GROUP);
-    constexpr int NW = dec_wring<BITS, GROUP>();
-    constexpr int NP = NW / 2;  // weight slots go in pairs: slot pair q serves lanes 2(q mod 2), 2(q mod 2) + 1
-    constexpr int NX = D_XRING;
-    static_assert(NW >= D_LANES && NW % D_LANES == 0 && NX % D_LANES == 0, "ring depths");
-    static_assert(BB % 16 == 0, "bulk copies move multiples of 16 bytes");
+    constexpr int SBW = sb_words(GROUP);
+    constexpr uint32_t XT = x_tile_bytes<NB>();
+    constexpr uint32_t SLOT = slot_bytes<BITS, GROUP, NB>();
+    constexpr int NS = ring_slots<BITS, GROUP, NB>();
+    static_assert(BB % 16 == 0 && SLOT % 128 == 0, "bulk copies move multiples of 16 bytes; tiles 128-aligned");
+    static_assert(NS >= 2, "at least two ring slots");
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;          // activation ring (1024-aligned for the swizzle)
-    const uint32_t wbase = base + (uint32_t)NX * D_X_BYTES;  // weight ring
-    const uint32_t ring_bytes = (uint32_t)NX * D_X_BYTES + (uint32_t)NW * BB;
-    DecSmem* sh = reinterpret_cast<DecSmem*>(smem_raw + (base - raw) + ring_bytes);
-    const uint32_t sh_addr = base + ring_bytes;
+    const uint32_t sh_addr = (raw + 127u) & ~127u;
+    DecSmem* sh = reinterpret_cast<DecSmem*>(smem_raw + (sh_addr - raw));
+    const uint32_t ring = sh_addr + D_RING0;  // slot s: two weight blocks, then two activation tiles
+    const int M = p.M;
 #define BAR(field, i) (sh_addr + (uint32_t)offsetof(DecSmem, field) + 8u * (uint32_t)(i))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -126,284 +213,123 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     for (int i = 1; i < p.nproj; ++i)
         if ((int)blockIdx.x >= p.proj[i].cta_begin) pi = i;
     const DecProj& P = p.proj[pi];
-    const int c = (int)blockIdx.x - P.cta_begin;
+    const int cta = (int)blockIdx.x - P.cta_begin;
     const int U = P.units, PC = P.nctas, KB = p.KB;
-    const int u0 = (int)((int64_t)c * U / PC);
-    const int u1 = (int)((int64_t)(c + 1) * U / PC);
+    const int u0 = (int)((int64_t)cta * U / PC);
+    const int u1 = (int)((int64_t)(cta + 1) * U / PC);
+    const int nblk = u1 - u0;
+    const int npairs = (nblk + 1) / 2;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NP; ++s) {
-            mbar_init(BAR(wfull, s), 1);
-            mbar_init(BAR(wempty, s), 8);  // the four warps of each of the pair's two groups read the codes
-        }
-        for (int s = 0; s < NX; ++s) {
-            mbar_init(BAR(xfull, s), 1);
-            mbar_init(BAR(xempty, s), 1);  // the block's MMAs read x
-        }
-        for (int l = 0; l < D_A_HALVES * D_LANES; ++l) {
-            mbar_init(BAR(a_full, l), 4);
-            mbar_init(BAR(a_empty, l), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(BAR(acc_full, b), D_LANES);  // every issuer commits at every segment end
-            mbar_init(BAR(acc_empty, b), 4);       // the four warps of the group draining it
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(BAR(full, s), 2);          // both producers
+            mbar_init(BAR(empty, s), D_CWARPS);  // every consumer warp
         }
         sh->abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == D_ISSUER0) tmem_alloc(sh_addr + (uint32_t)offsetof(DecSmem, tmem_base), D_TMEM_COLS);
-    // The activation tiles' rows M..15 stay zero for the whole launch: the
-    // TMA loads write rows 0..M-1 only (the tensor map's box is M rows).
-    for (uint32_t off = 16u * threadIdx.x; off < (uint32_t)NX * D_X_BYTES; off += 16u * D_THREADS)
-        sts_zero16(base + off);
-    fence_proxy_async_smem();  // generic-proxy zeros -> TMA writes and tensor-core reads
-    tc_fence_before();
+    // Activation rows M..8NB-1 stay zero for the whole launch: the TMA loads
+    // write rows 0..M-1 only (the tensor map's box is M rows).
+    for (int s = 0; s < NS; ++s)
+        for (uint32_t off = 16u * threadIdx.x; off < 2u * XT; off += 16u * D_THREADS)
+            sts_zero16(ring + (uint32_t)s * SLOT + 2u * BB + off);
+    fence_proxy_async_smem();  // generic-proxy zeros -> TMA writes
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = sh->tmem_base;
     volatile int* abort_flag = &sh->abort_flag;
     if (threadIdx.x == 0) pdl_launch_dependents();
 
-    if (warp == 0 || warp == D_WPROD1) {
-        // ---------------------------------------------------------- weights producers
-        // Blocks go in pairs (two consecutive blocks are contiguous, ~18 KB:
-        // a bulk copy moves data faster the larger it is), and two threads in
-        // two warps take alternate pairs.  The weights never depend on an
-        // earlier kernel, so these threads start before the grid dependency
-        // is resolved.
+    if (warp == D_WPROD || warp == D_XPROD) {
+        // ---------------------------------------------------------- producers
+        // The weights never depend on an earlier kernel, so their producer
+        // starts before the grid dependency is resolved; the activations may
+        // come from the previous kernel.
         if (lane == 0) {
-            const int pp = warp == 0 ? 0 : 1;
+            const bool wprod = warp == D_WPROD;
             const uint64_t policy = policy_evict_first();  // the weights are read once
-            const int n = u1 - u0;
-            for (int j = pp; 2 * j < n; j += 2) {
-                const int ps = j % NP;
-                const uint32_t ph = (uint32_t)((j / NP) & 1);
-                if (!wait_or_abort_lazy(BAR(wempty, ps), ph ^ 1u, abort_flag, p.status)) break;
-                const uint32_t bytes = (2 * j + 1 < n ? 2u : 1u) * (uint32_t)BB;
-                mbar_arrive_expect_tx(BAR(wfull, ps), bytes);
-                bulk_g2s_hint(wbase + (uint32_t)ps * (2u * BB), P.packed + (size_t)(u0 + 2 * j) * BB, bytes,
-                              BAR(wfull, ps), policy);
+            if (!wprod) {
+                prefetch_tmap(&xmap);
+                pdl_wait();
             }
-        }
-    } else if (warp == D_XPROD) {
-        // ---------------------------------------------------------- activations producer
-        if (lane == 0) {
-            prefetch_tmap(&xmap);
-            pdl_wait();  // x may come from the previous kernel
-            const uint32_t x_bytes = 2u * 64u * 2u * (uint32_t)p.M;  // two panels of M rows
-            int kb = u0 % KB;
-            for (int u = u0, i = 0; u < u1; ++u, ++i) {
-                const int s = i % NX;
-                const uint32_t ph = (uint32_t)((i / NX) & 1);
-                if (!wait_or_abort_lazy(BAR(xempty, s), ph ^ 1u, abort_flag, p.status)) break;
-                const uint32_t st = base + (uint32_t)s * D_X_BYTES;
-                mbar_arrive_expect_tx(BAR(xfull, s), x_bytes);
-                tma_load_2d(st, &xmap, kb * KBLK, 0, BAR(xfull, s));
-                tma_load_2d(st + D_X_PANEL, &xmap, kb * KBLK + 64, 0, BAR(xfull, s));
-                if (++kb == KB) kb = 0;
+            int issued = 0;
+            for (int j = 0; j < npairs; ++j) {
+                const int s = j % NS;
+                if (!wait_or_abort_lazy(BAR(empty, s), (uint32_t)((j / NS) & 1) ^ 1u, abort_flag, p.status)) break;
+                const int nb2 = min(2, nblk - 2 * j);
+                const uint32_t st = ring + (uint32_t)s * SLOT;
+                if (wprod) {
+                    const uint32_t bytes = (uint32_t)nb2 * BB;
+                    mbar_arrive_expect_tx(BAR(full, s), bytes);
+                    bulk_g2s_hint(st, P.packed + (size_t)(u0 + 2 * j) * BB, bytes, BAR(full, s), policy);
+                } else {
+                    mbar_arrive_expect_tx(BAR(full, s), (uint32_t)nb2 * D_XROW * (uint32_t)M);
+                    for (int h = 0; h < nb2; ++h)
+                        tma_load_2d(st + 2u * BB + (uint32_t)h * XT, &xmap, ((u0 + 2 * j + h) % KB) * KBLK, 0,
+                                    BAR(full, s));
+                }
+                issued = j + 1;
             }
-        }
-    } else if (warp < D_DEQ_WARP0) {
-        // ---------------------------------------------------------- MMA issuers
-        // Issuer e takes the blocks i = e (mod 4) of the run (the ones group e
-        // dequantizes into A buffer e) and accumulates them into chain e of
-        // the segment.  Every issuer waits for the segment's accumulators to
-        // be drained and commits at every segment end, so none runs a segment
-        // ahead of another.
-        if (lane == 0) {
-            const int e = warp - D_ISSUER0;
-            int seg = 0, seg_start = u0;
-            int kb = u0 % KB;
-            bool open = false;
-            for (int u = u0, i = 0; u < u1; ++u, ++i) {
-                const bool seg_end = (kb == KB - 1) || (u == u1 - 1);
-                const int db = seg & 1;
-                if (!open) {
-                    if (!wait_or_abort(BAR(acc_empty, db), (uint32_t)((seg >> 1) & 1) ^ 1u, abort_flag, p.status))
-                        break;
-                    open = true;
-                }
-                if ((i & (D_LANES - 1)) == e) {
-                    const int s = i % NX;
-                    const uint32_t ph = (uint32_t)((i / NX) & 1);
-                    const int jl = i / D_LANES;  // this lane's block count; its halves are 2 jl, 2 jl + 1
-                    if (!wait_or_abort(BAR(xfull, s), ph, abort_flag, p.status)) break;
-                    const int j = u - seg_start;  // block index within the segment
-                    const uint32_t dcol = tmem + D_ACC_COL0 + (uint32_t)(D_LANES * db + e) * D_MMA_N;
-                    const uint32_t acol = tmem + (uint32_t)e * D_A_COLS;
-                    const uint64_t bd0 = sw128_desc(base + (uint32_t)s * D_X_BYTES);
-                    bool ok = true;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {  // each half of the depth as soon as it is in TMEM
-                        const int t = 2 * jl + h;  // the lane's half number: buffer t mod 3, use t / 3
-                        const int b = t % D_A_HALVES;
-                        if (!wait_or_abort(BAR(a_full, D_A_HALVES * e + b), (uint32_t)((t / D_A_HALVES) & 1), abort_flag,
-                                           p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int k = 4 * h; k < 4 * h + 4; ++k) {
-                            // +32 bytes per 16-deep step, +2 KB per 64-deep panel (descriptor units of 16 bytes)
-                            const uint64_t bd = bd0 + (uint64_t)((k >> 2) * (D_X_PANEL >> 4) + (k & 3) * 2);
-                            umma_ts(dcol, acol + (uint32_t)b * D_A_HALF_COLS + 8u * (k - 4 * h), bd, D_IDESC,
-                                    (j < D_LANES && k == 0) ? 0u : 1u);
-                        }
-                        umma_commit(BAR(a_empty, D_A_HALVES * e + b));
-                    }
-                    if (!ok) break;
-                    umma_commit(BAR(xempty, s));
-                }
-                if (seg_end) {
-                    umma_commit(BAR(acc_full, db));  // this issuer's MMAs of the segment (maybe none)
-                    ++seg;
-                    open = false;
-                    seg_start = u + 1;
-                }
-                if (++kb == KB) kb = 0;
-            }
+            if (*abort_flag)  // no copy may still be landing when the CTA exits
+                for (int j = max(0, issued - NS); j < issued; ++j) (void)mbar_wait(BAR(full, j % NS), (uint32_t)((j / NS) & 1));
         }
     } else {
-        // ------------------------------------------ dequantization (+ epilogue)
-        const int g = (warp - D_DEQ_WARP0) >> 2;  // group: blocks i = g (mod 4)
-        const int q = warp & 3;                   // tensor-memory lanes 32q .. 32q + 31
-        const int n_in = 32 * q + lane;           // weight row of this thread within the tile
-        const int M = p.M;
-        const int tile0 = u0 / KB;
+        // ---------------------------------------------------------- consumers
+        const int g = lane >> 2, c = lane & 3;
+        const int r_lo = 16 * warp + g, r_hi = r_lo + 8;  // this thread's rows within the tile
+        // ldmatrix: lanes 8j .. 8j + 7 address matrix j's eight rows; matrix j
+        // of a pair of steps is (step 2p + j/2, k half j mod 2)
+        const uint32_t xlane = (uint32_t)(lane & 7) * D_XROW + (uint32_t)((lane >> 3) & 1) * 16u + (uint32_t)(lane >> 4) * 32u;
+        float acc[4 * NB];
+#pragma unroll
+        for (int e = 0; e < 4 * NB; ++e) acc[e] = 0.f;
         pdl_wait();  // y, the partials and the counters may still be in use by the previous kernel
-        for (int u = u0 + g, i = g; u < u1; u += D_LANES, i += D_LANES) {
-            const int ps = (i >> 1) % NP;  // pair slot of this block
-            const uint32_t ph = (uint32_t)(((i >> 1) / NP) & 1);
-            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(wfull, ps), ph, abort_flag, p.status))) break;
-            const uint32_t st = wbase + (uint32_t)ps * (2u * BB) + (uint32_t)(i & 1) * BB;
-            uint32_t cw[4 * BITS];
-            load_row_codes_smem<BITS>(st, n_in, cw);
-            uint32_t sbw[sb_words(GROUP)];
-            load_row_sb_smem<GROUP>(st + sb_offset(BITS, GROUP, n_in), sbw);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(wempty, ps));  // codes are in registers
-            // Each half of the row's depth goes to the next of the lane's three
-            // half-block A buffers, so the dequantization runs up to a block
-            // and a half ahead of the lane's MMAs.
-            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)g * D_A_COLS;
-            auto half = [&](auto hc) -> bool {
-                constexpr int H = decltype(hc)::value;
-                uint32_t w[32];
-                weight_pairs<BITS, GROUP, 32 * H, 32>(cw, sbw, w);
-                const int t = 2 * (i / D_LANES) + H;  // the lane's half number: buffer t mod 3, use t / 3
-                const int b = t % D_A_HALVES;
-                if (!__all_sync(0xffffffffu, wait_or_abort(BAR(a_empty, D_A_HALVES * g + b),
-                                                           (uint32_t)((t / D_A_HALVES) & 1) ^ 1u, abort_flag, p.status)))
-                    return false;
-                tc_fence_after();
-                tmem_st32(ta + (uint32_t)b * D_A_HALF_COLS, w);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(a_full, D_A_HALVES * g + b));
-                return true;
-            };
-            if (!half(std::integral_constant<int, 0>{})) break;
-            if (!half(std::integral_constant<int, 1>{})) break;
-
-            // ---- this block ends a tile segment: drain the accumulators
-            const int tile = u / KB;
-            const int kb = u - tile * KB;
-            if (!(kb == KB - 1 || u == u1 - 1)) continue;
-            const int seg = tile - tile0;
-            const int db = seg & 1;
-            const int seg_start = seg == 0 ? u0 : tile * KB;  // first block of the segment
-            const int len = u - seg_start + 1;
-            const int i_start = seg_start - u0;
-            if (!__all_sync(0xffffffffu,
-                            wait_or_abort(BAR(acc_full, db), (uint32_t)((seg >> 1) & 1), abort_flag, p.status)))
+        int kb = u0 % KB, tile = u0 / KB, seg_start = u0;
+        for (int j = 0; j < npairs; ++j) {
+            const int s = j % NS;
+            if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), (uint32_t)((j / NS) & 1), abort_flag, p.status)))
                 break;
-            tc_fence_after();
-            // chain l holds the segment's blocks with run index = l (mod 4);
-            // add the chains that received a block, in chain order
-            float v[D_MMA_N];
-            bool any = false;
-            const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + D_ACC_COL0 + (uint32_t)(D_LANES * db) * D_MMA_N;
+            const uint32_t st = ring + (uint32_t)s * SLOT;
+            const bool pair = 2 * j + 1 < nblk;
 #pragma unroll
-            for (int l = 0; l < D_LANES; ++l) {
-                const bool used = len >= D_LANES || ((l - i_start) & (D_LANES - 1)) < len;
-                uint32_t r[16];
-                tmem_ld16(trow + (uint32_t)l * D_MMA_N, r);
-                if (used) {
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !pair) break;
+                const uint32_t blk = st + (uint32_t)h * BB;
+                uint32_t wl[BITS], wh[BITS], sl[SBW], sh2[SBW];
+                load_class_words_smem<BITS>(blk, r_lo, c, wl);
+                load_class_words_smem<BITS>(blk, r_hi, c, wh);
+                load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, r_lo), sl);
+                load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, r_hi), sh2);
+                uint32_t b[NB][8][2];
+                load_x_frags<NB>(st + 2u * BB + (uint32_t)h * XT + xlane, b);
+                if (h == 1 || !pair) {  // every read of the slot is issued: release it
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(empty, s));
+                }
+                mma_steps<BITS, GROUP, NB>(wl, wh, sl, sh2, b, acc);
+                const int u = u0 + 2 * j + h;
+                if (kb == KB - 1 || u == u1 - 1) {  // this block ends a tile segment
+                    segment_end<NB>(p, P, acc, tile, (seg_start == tile * KB) && (kb == KB - 1), seg_start == u0, cta,
+                                    U, PC, KB, M, warp, lane, r_lo, c);
 #pragma unroll
-                    for (int e2 = 0; e2 < D_MMA_N; ++e2) v[e2] = any ? v[e2] + __uint_as_float(r[e2]) : __uint_as_float(r[e2]);
-                    any = true;
+                    for (int e = 0; e < 4 * NB; ++e) acc[e] = 0.f;
+                    seg_start = u + 1;
+                }
+                if (++kb == KB) {
+                    kb = 0;
+                    ++tile;
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(acc_empty, db));  // accumulators drained
-            const int64_t n = (int64_t)tile * TILE_N + n_in;
-            const bool whole = (seg_start == tile * KB) && (kb == KB - 1);
-            if (whole) {
-                if (n < P.N)
-                    for (int m = 0; m < M; ++m)
-                        P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v[m]));
-                continue;
-            }
-            // publish this run's partial of the tile; the last run to arrive
-            // adds them all in run (k) order
-            const int slot = P.slot_begin + 2 * c + (seg_start == u0 ? 0 : 1);
-            float4* sp = reinterpret_cast<float4*>(p.partials + ((size_t)slot * TILE_N + n_in) * D_MMA_N);
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) __stcg(sp + e2, make_float4(v[4 * e2], v[4 * e2 + 1], v[4 * e2 + 2], v[4 * e2 + 3]));
-            __syncwarp();
-            unsigned prev = 0;
-            unsigned* ctr = &p.counters[(size_t)(P.ctr_begin + tile) * 4 + q];
-            if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
-            __syncwarp();
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            const int t0 = tile * KB, t1 = t0 + KB - 1;
-            const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
-            if (prev != (unsigned)(cl - cf)) continue;
-            float acc[D_MMA_N];
-#pragma unroll
-            for (int e2 = 0; e2 < D_MMA_N; ++e2) acc[e2] = 0.f;
-            for (int cb = cf; cb <= cl; ++cb) {
-                const int b0 = (int)((int64_t)cb * U / PC);
-                const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
-                const float4* cp = reinterpret_cast<const float4*>(p.partials + ((size_t)sc * TILE_N + n_in) * D_MMA_N);
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    const float4 f = __ldcg(cp + e2);
-                    acc[4 * e2] += f.x;
-                    acc[4 * e2 + 1] += f.y;
-                    acc[4 * e2 + 2] += f.z;
-                    acc[4 * e2 + 3] += f.w;
-                }
-            }
-            if (n < P.N)
-                for (int m = 0; m < M; ++m) P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
-            if (lane == 0) *ctr = 0u;
         }
     }
 #undef BAR
-    // teardown: every role has left its loop and nothing is in flight
-    __syncwarp();
-    tc_fence_before();
+    // teardown: every role has left its loop; after an abort the producers
+    // have waited for the copies they issued
     __syncthreads();
-    if (warp == D_ISSUER0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, D_TMEM_COLS);
-    }
-}
-
-template <int BITS, int GROUP>
-size_t dec_smem() {
-    return (size_t)D_XRING * D_X_BYTES + (size_t)dec_wring<BITS, GROUP>() * block_bytes(BITS, GROUP) + sizeof(DecSmem) +
-           1024;
 }
 
 template <int BITS, int GROUP>
 cudaError_t launch_bg(const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    const size_t smem = dec_smem<BITS, GROUP>();
-    return launch_pdl(decode_kernel<BITS, GROUP>, grid, D_THREADS, smem, st, p, map);
+    if (p.M > 8) return launch_pdl(decode_kernel<BITS, GROUP, 2>, grid, D_THREADS, (size_t)D_SMEM, st, p, map);
+    return launch_pdl(decode_kernel<BITS, GROUP, 1>, grid, D_THREADS, (size_t)D_SMEM, st, p, map);
 }
 
 template <int BITS>
@@ -413,24 +339,44 @@ cudaError_t launch_b(int group, const DecParams& p, const CUtensorMap& map, int 
     return launch_bg<BITS, 128>(p, map, grid, st);
 }
 
+// The kernel's shared-memory limit, the largest shared-memory carveout (two
+// CTAs of 110 KB per SM), and how many CTAs of it an SM holds (min over the
+// instantiations, which differ only in registers).
+template <int BITS, int GROUP, int NB>
+cudaError_t allow_bgn(int* per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<BITS, GROUP, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)D_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_kernel<BITS, GROUP, NB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS, GROUP, NB>, D_THREADS, (size_t)D_SMEM);
+    if (e != cudaSuccess) return e;
+    *per_sm = min(*per_sm, n);
+    return cudaSuccess;
+}
 template <int BITS, int GROUP>
-cudaError_t allow_bg() {
-    return cudaFuncSetAttribute(decode_kernel<BITS, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)dec_smem<BITS, GROUP>());
+cudaError_t allow_bg(int* per_sm) {
+    cudaError_t e = allow_bgn<BITS, GROUP, 1>(per_sm);
+    return e != cudaSuccess ? e : allow_bgn<BITS, GROUP, 2>(per_sm);
 }
 
 template <int BITS>
-cudaError_t allow_b() {
-    for (cudaError_t e : {allow_bg<BITS, 32>(), allow_bg<BITS, 64>(), allow_bg<BITS, 128>()})
+cudaError_t allow_b(int* per_sm) {
+    for (cudaError_t e : {allow_bg<BITS, 32>(per_sm), allow_bg<BITS, 64>(per_sm), allow_bg<BITS, 128>(per_sm)})
         if (e != cudaSuccess) return e;
     return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t decode_allow_smem() {
-    for (cudaError_t e : {allow_b<2>(), allow_b<3>(), allow_b<4>(), allow_b<5>(), allow_b<6>(), allow_b<8>()})
+cudaError_t decode_allow_smem(int* ctas_per_sm) {
+    int n = D_CTAS_PER_SM;
+    for (cudaError_t e : {allow_b<2>(&n), allow_b<3>(&n), allow_b<4>(&n), allow_b<5>(&n), allow_b<6>(&n), allow_b<8>(&n)})
         if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    *ctas_per_sm = n;
     return cudaSuccess;
 }
 

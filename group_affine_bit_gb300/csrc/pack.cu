@@ -36,13 +36,16 @@ __global__ void __launch_bounds__(TILE_N) pack_kernel(int group, int64_t N, int6
         const int shift_in = plane ? P0 : 0;
         const uint32_t fmask = (1u << p) - 1u;
         for (int w = 0; w < 4 * p; ++w) {
+            // class-major words: word p*c + v holds class c's pairs j = v*(16/p) + i,
+            // pair C = 4j + c at k = 2C
+            const int c = w / p, v = w % p;
             uint32_t word = 0;
             for (int i = 0; i < 16 / p; ++i) {
-                const int k0 = w * (32 / p) + 2 * i;
+                const int k0 = 2 * (4 * (v * (16 / p) + i) + c);
                 word |= ((code(k0) >> shift_in) & fmask) << (p * i);
                 word |= ((code(k0 + 1) >> shift_in) & fmask) << (16 + p * i);
             }
-            *reinterpret_cast<uint32_t*>(out + chunk_offset(BITS, plane, n, w / 4) + 4 * (w % 4)) = word;
+            *reinterpret_cast<uint32_t*>(out + word_offset(BITS, plane, n, w)) = word;
         }
     }
     const int gw = sb_words(group);

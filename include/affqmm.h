@@ -175,7 +175,7 @@ AFFQMM_API int affqmm_workspace_status(void* workspace, void* stream);
 
 /* Largest M affqmm_run_noalloc takes, and the size of its built-in scratch. */
 #define AFFQMM_NOALLOC_MAX_M 16
-#define AFFQMM_NOALLOC_SCRATCH_BYTES (3u << 20)
+#define AFFQMM_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* affqmm_run for M <= 16 activation rows without any device memory from the
  * caller beyond x and y.  The paper has no counterpart to this entry point:
@@ -186,7 +186,7 @@ AFFQMM_API int affqmm_workspace_status(void* workspace, void* stream);
  * its plug-ins no allocator, or a latency-critical loop that must not call
  * cudaMalloc/cudaFree (they can synchronize the device) once it has started.
  * Such callers cannot supply the workspace affqmm_run wants, so this call
- * uses a scratch array of AFFQMM_NOALLOC_SCRATCH_BYTES (3 MiB) that the
+ * uses a scratch array of AFFQMM_NOALLOC_SCRATCH_BYTES (8 MiB) that the
  * library itself places in device memory; every GPU that loads the library
  * holds it until the process exits.  The call allocates nothing: no
  * cudaMalloc, no cudaFree, no allocating library routine.
