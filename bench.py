@@ -19,8 +19,9 @@ so that the bytes touched between two reads of one copy exceed the 129 MB L2.
 Steps are replayed from CUDA graphs and timed with CUDA events on the stream
 that launches them.  `e2e` times the same steps through the Python API with
 the activations uploaded from pinned host memory and the outputs read back
-every step.  `--impl reference` times the CPU oracle on a bounded sample of
-the same workload on the host cores.  Under torchrun every rank runs an
+every step (AFFQMM_E2E_HOST_CALL=1: through affqmm_run_host instead, one C
+call per projection with host buffers).  `--impl reference` times the CPU
+oracle on a bounded sample of the same workload on the host cores.  Under torchrun every rank runs an
 independent replica (the path needs no exchange) and rank 0 reports the
 aggregate over ranks with the slowest rank's time.
 """
@@ -214,6 +215,10 @@ class Case:
     def run(self, i: int, workspace):
         self.api.run(self.ws[i % self.copies], self.x, y=self.y, workspace=workspace)
 
+    def run_host(self, i: int, workspace, x_host, y_host):
+        """One C call: x from host memory into self.x, the projection, self.y back to y_host."""
+        self.api.run_host(self.ws[i % self.copies], x_host, y_host, self.x, self.y, workspace=workspace)
+
     @property
     def packed_bytes(self) -> int:   # codes + bf16 scale and bias per group
         return self.N * self.K * self.bits // 8 + 4 * self.N * self.K // self.group
@@ -257,6 +262,11 @@ class Workload:
     def step(self, i: int):
         for c in self.cases:
             c.run(i, self.workspace)
+
+    def step_host(self, i: int, h_in, h_out):
+        """The step through affqmm_run_host: each case's x from host memory, y back to it."""
+        for c, hx, hy in zip(self.cases, h_in, h_out):
+            c.run_host(i, self.workspace, hx, hy)
 
     @property
     def launches_per_step(self) -> int:
@@ -426,6 +436,7 @@ class EmbedRows(Workload):
 
     launches_per_step = 1
     kernels_per_step = 1
+    step_host = None  # no host-buffer entry point: e2e uploads the ids and reads the rows back with torch copies
 
     @property
     def packed_row_bytes(self) -> int:
@@ -513,8 +524,9 @@ def sustain_for_clocks(graphs, device, seconds: float = 1.0):
 
 
 def time_e2e(wl, steps: int, device):
-    """Same steps through the Python API, activations uploaded from pinned host
-    memory and outputs read back to pinned host memory every step."""
+    """Same steps through the public API with host buffers: activations uploaded
+    from pinned host memory and outputs read back to pinned host memory every
+    step, inside the timed region."""
     import torch
     ins, outs = wl.e2e_io()
     h_in = [t.detach().cpu().pin_memory() for t in ins]
@@ -522,6 +534,9 @@ def time_e2e(wl, steps: int, device):
     bi = sum(t.numel() * t.element_size() for t in h_in)
     bo = sum(t.numel() * t.element_size() for t in h_out)
     stream = torch.cuda.current_stream(device)
+    # The C call with host buffers (affqmm_run_host, `wl.step_host`) measured slower on GB300 than torch's
+    # copies around affqmm_run (1760 against 2586 GB/s on the 241-launch decode step), so the copies stay.
+    host_call = getattr(wl, "step_host", None) if os.environ.get("AFFQMM_E2E_HOST_CALL") == "1" else None
     for i in range(3):
         wl.step(i)
     torch.cuda.synchronize(device)
@@ -530,6 +545,9 @@ def time_e2e(wl, steps: int, device):
     t0 = time.perf_counter()
     e0.record(stream)
     for i in range(steps):
+        if host_call is not None:
+            host_call(i, h_in, h_out)
+            continue
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
         wl.step(i)

@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             "affqmm_dequant": (i32, [wp, vp, vp]),
             "affqmm_workspace_status": (i32, [vp, vp]),
             "affqmm_run_noalloc": (i32, [wp, vp, i64, vp, vp]),
+            "affqmm_run_host": (i32, [wp, vp, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]),
             "affqmm_embed_rows": (i32, [wp, vp, i64, i32, ctypes.c_uint16, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -212,6 +213,32 @@ def run(w: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, workspa
     cw = w.cstruct()
     _check(lib().affqmm_run(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), buf.data_ptr() if need else None,
                             buf.numel(), sp), "affqmm_run")
+    return y
+
+
+def run_host(w: PackedWeight, x: torch.Tensor, y: torch.Tensor, x_dev: torch.Tensor, y_dev: torch.Tensor,
+             workspace: Workspace | None = None, stream=None) -> torch.Tensor:
+    """affqmm_run_host: x (host, bf16 [M, K]) is copied into x_dev, the projection
+    runs into y_dev, and y_dev is copied back into y (host, bf16 [M, N]), all on
+    the stream.  Pinned host tensors keep the copies asynchronous; y is complete
+    once the stream has passed the call."""
+    M = x.shape[0]
+    if (x.is_cuda or y.is_cuda or x.dtype != torch.bfloat16 or y.dtype != torch.bfloat16
+            or tuple(x.shape) != (M, w.K) or tuple(y.shape) != (M, w.N)
+            or not x.is_contiguous() or not y.is_contiguous()):
+        raise ValueError(f"x and y must be contiguous host bf16 tensors [M, {w.K}] and [M, {w.N}]")
+    _check_x(x_dev, w.K)
+    if (x_dev.shape[0] != M or y_dev.dtype != torch.bfloat16 or tuple(y_dev.shape) != (M, w.N)
+            or not y_dev.is_contiguous() or y_dev.device != x_dev.device):
+        raise ValueError(f"x_dev and y_dev must be contiguous bf16 [M, {w.K}] and [M, {w.N}] on one device")
+    dev = x_dev.get_device()
+    sp = _stream_ptr(stream, dev)
+    ws = workspace or default_workspace(dev, sp)
+    need = workspace_bytes(w, M)
+    buf = ws.get(need)
+    cw = w.cstruct()
+    _check(lib().affqmm_run_host(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), x_dev.data_ptr(), y_dev.data_ptr(),
+                                 buf.data_ptr() if need else None, buf.numel(), sp), "affqmm_run_host")
     return y
 
 

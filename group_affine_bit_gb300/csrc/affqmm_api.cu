@@ -144,6 +144,29 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
+// The driver's asynchronous host<->device copies, fetched at run time like
+// the tensor-map encoder: the driver, which registered the caller's
+// page-locked buffers, decides whether a copy can run asynchronously.
+using CopyHtoDFn = CUresult (*)(CUdeviceptr, const void*, size_t, CUstream);
+using CopyDtoHFn = CUresult (*)(void*, CUdeviceptr, size_t, CUstream);
+template <typename Fn>
+Fn driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(f);
+}
+CopyHtoDFn copy_htod() {
+    static CopyHtoDFn fn = driver_fn<CopyHtoDFn>("cuMemcpyHtoDAsync");
+    return fn;
+}
+CopyDtoHFn copy_dtoh() {
+    static CopyDtoHFn fn = driver_fn<CopyDtoHFn>("cuMemcpyDtoHAsync");
+    return fn;
+}
+
 // x [M, K] bf16 row-major as 64 (k) x 128-row boxes with the 128-byte
 // swizzle the tensor core reads (the prompt kernel); rows past M and k past
 // K read as zero.
@@ -390,6 +413,42 @@ int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint16_t* x, in
                        void* workspace, size_t ws_bytes, void* stream) {
     if (!ys) return AFFQMM_E_NULL;
     return run_impl(count, ws, x, M, ys, workspace, ws_bytes, stream);
+}
+
+int affqmm_run_host(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y, uint16_t* x_dev,
+                    uint16_t* y_dev, void* workspace, size_t ws_bytes, void* stream) {
+    int rc = check_weight(w);
+    if (rc) return rc;
+    if (M < 0 || M > AFFQMM_MAX_M) return AFFQMM_E_M;
+    if (M == 0 || w->N == 0) return AFFQMM_OK;
+    if (!y || !y_dev) return AFFQMM_E_NULL;
+    if (!aligned(y_dev, 2)) return AFFQMM_E_ALIGN;
+    if (w->K > 0) {
+        if (!x || !x_dev) return AFFQMM_E_NULL;
+        if (!aligned(x_dev, 16)) return AFFQMM_E_ALIGN;
+    }
+    DeviceInfo* d = nullptr;
+    rc = device_info(&d);
+    if (rc) return rc;
+    size_t need = 0;
+    rc = workspace_for(1, w, M, &need);
+    if (rc) return rc;
+    if (need > 0) {
+        if (!workspace || ws_bytes < need) return AFFQMM_E_WORKSPACE;
+        if (!aligned(workspace, 256)) return AFFQMM_E_ALIGN;
+    }
+    CopyHtoDFn htod = copy_htod();
+    CopyDtoHFn dtoh = copy_dtoh();
+    if (!htod || !dtoh) return AFFQMM_E_CUDA;
+    CUstream cs = static_cast<CUstream>(stream);
+    if (w->K > 0 && htod(reinterpret_cast<CUdeviceptr>(x_dev), x, (size_t)M * (size_t)w->K * 2, cs) != CUDA_SUCCESS)
+        return AFFQMM_E_CUDA;
+    uint16_t* ys[1] = {y_dev};
+    rc = run_impl(1, w, x_dev, M, ys, workspace, ws_bytes, stream);
+    if (rc) return rc;
+    if (dtoh(y, reinterpret_cast<CUdeviceptr>(y_dev), (size_t)M * (size_t)w->N * 2, cs) != CUDA_SUCCESS)
+        return AFFQMM_E_CUDA;
+    return AFFQMM_OK;
 }
 
 int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* stream) {

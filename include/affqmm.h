@@ -146,6 +146,24 @@ AFFQMM_API int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, 
 AFFQMM_API int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M,
                        uint16_t* const* ys, void* workspace, size_t ws_bytes, void* stream);
 
+/* affqmm_run with the activations and outputs in host memory, the whole
+ * step of a caller that keeps x and y on the host: x is copied into x_dev,
+ * the projection runs, y_dev is copied back into y -- all enqueued on
+ * `stream` in that order (cudaMemcpyAsync, one copy each way).
+ *   x        host, bf16 [M, K] row-major (page-locked memory keeps the copy
+ *            asynchronous; pageable memory works and makes it synchronous)
+ *   y        host, bf16 [M, N] row-major; complete once the stream reaches
+ *            the end of the call
+ *   x_dev    device, bf16 [M, K], 16-byte aligned: where x is staged
+ *   y_dev    device, bf16 [M, N], 2-byte aligned: where y is computed
+ *   w, M, workspace, ws_bytes, stream   as affqmm_run
+ * The host buffers must stay valid until the stream has passed the call.
+ * y equals affqmm_run on the same inputs bit for bit.  Every argument is
+ * checked before anything is enqueued.
+ * Errors: as affqmm_run (x_dev, y_dev and the host pointers each NULL-checked). */
+AFFQMM_API int affqmm_run_host(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y, uint16_t* x_dev,
+                               uint16_t* y_dev, void* workspace, size_t ws_bytes, void* stream);
+
 /* Test hook: write the dequantized weights W (bf16 [N, K] row-major, device,
  * 2-byte aligned) with the same device arithmetic the run kernels use.
  * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_CUDA. */

@@ -95,6 +95,25 @@ def test_run_refusals_before_any_launch(L):
     assert _run(L, _w(), M=0) == 0
 
 
+def test_run_host_refusals_before_anything_is_enqueued(L):
+    names = api.STATUS_NAMES
+    w = _w()
+
+    def run_host(wp, x=0x10000, M=1, y=0x20000, x_dev=0x200000, y_dev=0x300000):
+        return L.affqmm_run_host(wp, x, M, y, x_dev, y_dev, None, 0, None)
+
+    assert names[run_host(None)] == "AFFQMM_E_NULL"
+    assert names[run_host(ctypes.byref(_w(bits=7)))] == "AFFQMM_E_BITS"
+    assert names[run_host(ctypes.byref(w), M=-1)] == "AFFQMM_E_M"
+    assert names[run_host(ctypes.byref(w), x=0)] == "AFFQMM_E_NULL"
+    assert names[run_host(ctypes.byref(w), y=0)] == "AFFQMM_E_NULL"
+    assert names[run_host(ctypes.byref(w), x_dev=0)] == "AFFQMM_E_NULL"
+    assert names[run_host(ctypes.byref(w), y_dev=0)] == "AFFQMM_E_NULL"
+    assert names[run_host(ctypes.byref(w), x_dev=0x200008)] == "AFFQMM_E_ALIGN"
+    assert names[run_host(ctypes.byref(w), y_dev=0x300001)] == "AFFQMM_E_ALIGN"
+    assert run_host(ctypes.byref(w), M=0) == 0
+
+
 def test_stacked_refusals(L):
     names = api.STATUS_NAMES
     arr = (api.CWeight * 2)(_w(), _w(K=512))
