@@ -57,7 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default: per workload)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="gate_up_decode",
-                    choices=["gate_up_decode", "decode_step", "prompt_chunk", "lane_sweep", "tiny", "embed_rows"])
+                    choices=["gate_up_decode", "decode_step", "prompt_chunk", "lane_sweep", "tiny", "embed_rows",
+                             "gate_up_exact"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -212,8 +213,13 @@ class Case:
         self.x = synth.activations(M, K, g, device)
         self.y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
 
+    exact = False  # the exact-codes form (affqmm_run_exact) instead of rounded weights
+
     def run(self, i: int, workspace):
-        self.api.run(self.ws[i % self.copies], self.x, y=self.y, workspace=workspace)
+        if self.exact:
+            self.api.run_exact(self.ws[i % self.copies], self.x, y=self.y, workspace=workspace)
+        else:
+            self.api.run(self.ws[i % self.copies], self.x, y=self.y, workspace=workspace)
 
     def run_host(self, i: int, workspace, x_host, y_host):
         """One C call: x from host memory into self.x, the projection, self.y back to y_host."""
@@ -332,6 +338,18 @@ class GateUpDecode(Workload):
     def describe(self):
         c = self.cases[0]
         return f"{self.name}: M={c.M} K={c.K} N={c.N} {c.bits}-bit group {c.group}"
+
+
+class GateUpExact(GateUpDecode):
+    """The gate/up decode shape through the exact-codes form (the pages' lane
+    projection: exact codes, group sums of x)."""
+    name = "gate_up_exact"
+
+    def make_cases(self, api, synth, device, shape=None):
+        cases = super().make_cases(api, synth, device, shape)
+        for c in cases:
+            c.exact = True
+        return cases
 
 
 class Tiny(GateUpDecode):
@@ -465,7 +483,7 @@ class EmbedRows(Workload):
 
 
 WORKLOADS = {"gate_up_decode": GateUpDecode, "decode_step": DecodeStep, "prompt_chunk": PromptChunk,
-             "lane_sweep": LaneSweep, "tiny": Tiny, "embed_rows": EmbedRows}
+             "lane_sweep": LaneSweep, "tiny": Tiny, "embed_rows": EmbedRows, "gate_up_exact": GateUpExact}
 
 
 # ----------------------------------------------------------------------------- timing
@@ -578,6 +596,9 @@ class OracleSample:
         self.sb, self.bb = synth.bits_u16(s), synth.bits_u16(b)
         self.threads = host_cores()
         self.embed = bool(shape.get("embed"))
+        self.exact = bool(shape.get("exact"))
+        if self.exact:
+            self.threads = 1  # the exact-codes oracle is not threaded
         if self.embed:
             self.threads = 1
             self.embed_scale = int(synth.bits_u16(torch_bf16_scalar(math.sqrt(self.K)))[0])
@@ -596,6 +617,8 @@ class OracleSample:
             ids = np.arange(rows, dtype=np.int32)
             self.orc.embed_rows(self.bits, self.group, self.cb[:rows], self.sb[:rows], self.bb[:rows], ids,
                                 self.embed_scale)
+        elif self.exact:
+            self.orc.qmm_groupsum(self.bits, self.group, self.xb, self.cb[:rows], self.sb[:rows], self.bb[:rows])
         else:
             self.orc.qmm(self.bits, self.group, self.xb, self.cb[:rows], self.sb[:rows], self.bb[:rows],
                          nthreads=self.threads)
@@ -610,6 +633,9 @@ class OracleSample:
         if self.embed:
             return (f"{reps} x {rows} gathered rows of K={self.K}, {self.bits}-bit g{self.group} times a bf16 "
                     f"scale; oracle on one thread")
+        if self.exact:
+            return (f"{reps} x {rows} of {self.N} output rows of one projection of the workload (M={self.M}, "
+                    f"K={self.K}, {self.bits}-bit g{self.group}); float64 exact-codes oracle on one thread")
         return (f"{reps} x {rows} of {self.N} output rows of one projection of the workload (M={self.M}, "
                 f"K={self.K}, {self.bits}-bit g{self.group}); float64 oracle threaded over rows")
 
@@ -632,6 +658,7 @@ WORKLOAD_ORACLE_SHAPES = {   # the projection each workload's oracle sample take
     "lane_sweep": lambda s: dict(bits=4, group=64, M=2, N=s.SWEEP_SHAPE["N"], K=s.SWEEP_SHAPE["K"],
                                  seed=s.SWEEP_SHAPE["seed"]),
     "embed_rows": lambda s: dict(bits=4, group=64, M=1, N=4096, K=s.HEAD_SHAPE[1], seed=s.EMBED_SEED, embed=True),
+    "gate_up_exact": lambda s: dict(s.GATE_UP_DECODE, exact=True),
 }
 
 

@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             "affqmm_workspace_status": (i32, [vp, vp]),
             "affqmm_run_noalloc": (i32, [wp, vp, i64, vp, vp]),
             "affqmm_run_host": (i32, [wp, vp, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]),
+            "affqmm_run_exact": (i32, [wp, vp, i64, vp, vp, ctypes.c_size_t, vp]),
             "affqmm_embed_rows": (i32, [wp, vp, i64, i32, ctypes.c_uint16, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -213,6 +214,25 @@ def run(w: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, workspa
     cw = w.cstruct()
     _check(lib().affqmm_run(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), buf.data_ptr() if need else None,
                             buf.numel(), sp), "affqmm_run")
+    return y
+
+
+def run_exact(w: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, workspace: Workspace | None = None,
+              stream=None) -> torch.Tensor:
+    """affqmm_run_exact (M <= 16): y = bf16(sum_g s_g * sum q x + b_g * sum x), the
+    exact-codes form (the weights are not rounded to bf16)."""
+    _check_x(x, w.K)
+    M = x.shape[0]
+    dev = x.get_device()
+    if y is None:
+        y = torch.empty(M, w.N, dtype=torch.bfloat16, device=x.device)
+    sp = _stream_ptr(stream, dev)
+    ws = workspace or default_workspace(dev, sp)
+    need = workspace_bytes(w, M)
+    buf = ws.get(need)
+    cw = w.cstruct()
+    _check(lib().affqmm_run_exact(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), buf.data_ptr() if need else None,
+                                  buf.numel(), sp), "affqmm_run_exact")
     return y
 
 

@@ -273,10 +273,10 @@ int check_stack(int count, const affqmm_weight* ws) {
 }
 
 int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, uint16_t* const* ys,
-             void* workspace, size_t ws_bytes, void* stream) {
+             void* workspace, size_t ws_bytes, void* stream, bool exact = false) {
     int rc = check_stack(count, ws);
     if (rc) return rc;
-    if (M < 0 || M > AFFQMM_MAX_M) return AFFQMM_E_M;
+    if (M < 0 || M > AFFQMM_MAX_M || (exact && M > kDecodeRows)) return AFFQMM_E_M;
     if (M == 0) return AFFQMM_OK;
     const int64_t K = ws[0].K;
     int64_t total_n = 0;
@@ -313,10 +313,12 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         if (rc) return rc;
         bind_workspace(&plan, workspace);
         for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i];
+        plan.p.x = x;
         CUtensorMap map;
         rc = make_x_map_decode(x, M, K, &map);
         if (rc) return rc;
-        if (launch_decode(ws[0].bits, ws[0].group, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
+        if (launch_decode(ws[0].bits, ws[0].group, plan.p, map, plan.grid, st, exact) != cudaSuccess)
+            return AFFQMM_E_CUDA;
         return AFFQMM_OK;
     }
     // Prompt rows: chunks of up to 128 rows on the tensor-core kernel.
@@ -407,6 +409,12 @@ int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y
                size_t ws_bytes, void* stream) {
     uint16_t* ys[1] = {y};
     return run_impl(1, w, x, M, ys, workspace, ws_bytes, stream);
+}
+
+int affqmm_run_exact(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y, void* workspace,
+                     size_t ws_bytes, void* stream) {
+    uint16_t* ys[1] = {y};
+    return run_impl(1, w, x, M, ys, workspace, ws_bytes, stream, true);
 }
 
 int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, uint16_t* const* ys,
@@ -572,6 +580,7 @@ extern "C" int affqmm_run_noalloc(const affqmm_weight* w, const uint16_t* x, int
     if (cudaMemsetAsync(scratch, 0, zeroed, st) != cudaSuccess) return AFFQMM_E_CUDA;
     bind_workspace(&plan, scratch);
     plan.p.proj[0].y = y;
+    plan.p.x = x;
     CUtensorMap map;
     rc = make_x_map_decode(x, M, w->K, &map);
     if (rc) return rc;

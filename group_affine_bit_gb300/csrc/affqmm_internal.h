@@ -35,6 +35,7 @@ struct DecParams {
     int32_t KB;              // k-blocks of 128
     int64_t K;
     int32_t M;               // activation rows (1..16)
+    const uint16_t* x;       // x [M, K] bf16 (read directly in exact-codes mode)
     uint32_t* status;        // device status word (bit 0: a bounded wait gave up)
     uint32_t* counters;
     float* partials;         // slot = 128 rows x 16 floats
@@ -108,7 +109,8 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, int threads, size_t
 // swizzle.  decode_allow_smem sets the kernels' shared-memory attributes and
 // reports how many decode CTAs one SM holds.
 cudaError_t decode_allow_smem(int* ctas_per_sm);
-cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st);
+cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st,
+                          bool exact = false);
 // prompt.cu: the tensor map describes x [M, K] bf16 with a 64 x 128 box.
 cudaError_t prompt_allow_smem();
 cudaError_t launch_prompt(int bits, const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st);

@@ -71,8 +71,11 @@ static_assert(sizeof(DecSmem) <= D_RING0, "barriers fit below the ring");
 
 template <int NB>
 constexpr uint32_t x_tile_bytes() { return 8u * NB * D_XROW; }  // 8 rows per activation block of the mma
+constexpr uint32_t D_XSUM = 256;  // per block, exact-codes mode: sums of x over each group, [4 groups][16 rows] fp32
 template <int BITS, int GROUP, int NB>
-constexpr uint32_t slot_bytes() { return 2u * (uint32_t)block_bytes(BITS, GROUP) + 2u * x_tile_bytes<NB>(); }
+constexpr uint32_t slot_bytes() {
+    return 2u * (uint32_t)block_bytes(BITS, GROUP) + 2u * x_tile_bytes<NB>() + 2u * D_XSUM;
+}
 template <int BITS, int GROUP, int NB>
 constexpr int ring_slots() {
     return (int)((D_SMEM - 128u - D_RING0) / slot_bytes<BITS, GROUP, NB>()) > D_SLOTS_MAX
@@ -118,6 +121,47 @@ __device__ __forceinline__ void mma_steps(const uint32_t* wl, const uint32_t* wh
         mma_steps<BITS, GROUP, NB, S + 1>(wl, wh, sl, sh, b, acc);
     }
 }
+// Exact-codes mode (the pages' lane projection): the A fragment holds the
+// exact codes q (no rounding of s*q + b), the mmas of one group accumulate
+// sum_k q x in accg, and at the group's end
+//     acc += s_row * accg + b_row * sum_{k in group} x[m, k]
+// with the group sums xs (fp32 [group][16 rows]) written by the activation
+// producer.  sl/sh hold the rows' s | b << 16 words.
+template <int BITS, int GROUP, int NB, int S = 0>
+__device__ __forceinline__ void mma_steps_exact(const uint32_t* wl, const uint32_t* wh, const uint32_t* sl,
+                                                const uint32_t* sh, const uint32_t (&b)[NB][8][2], uint32_t xs, int c,
+                                                float* acc, float* accg) {
+    if constexpr (S < 8) {
+        constexpr int P0 = plane0_bits(BITS);
+        const uint32_t a0 = class_code_pair<BITS, 2 * S>(wl, wl + P0);
+        const uint32_t a1 = class_code_pair<BITS, 2 * S>(wh, wh + P0);
+        const uint32_t a2 = class_code_pair<BITS, 2 * S + 1>(wl, wl + P0);
+        const uint32_t a3 = class_code_pair<BITS, 2 * S + 1>(wh, wh + P0);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_bf16(accg + 4 * nb, a0, a1, a2, a3, b[nb][S][0], b[nb][S][1]);
+        constexpr int SPG = GROUP / 16;  // 16-deep steps per group
+        if constexpr ((S + 1) % SPG == 0) {
+            constexpr int GI = S / SPG;
+            const float s_lo = __uint_as_float(sl[GI] << 16), b_lo = __uint_as_float(sl[GI] & 0xFFFF0000u);
+            const float s_hi = __uint_as_float(sh[GI] << 16), b_hi = __uint_as_float(sh[GI] & 0xFFFF0000u);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                uint32_t x0u, x1u;  // the group sums of activation rows 8nb + 2c, 8nb + 2c + 1
+                lds_v2(xs + (uint32_t)(GI * 16 + 8 * nb + 2 * c) * 4u, x0u, x1u);
+                const float x0 = __uint_as_float(x0u), x1 = __uint_as_float(x1u);
+                float* a = acc + 4 * nb;
+                float* q = accg + 4 * nb;
+                a[0] = fmaf(b_lo, x0, fmaf(s_lo, q[0], a[0]));
+                a[1] = fmaf(b_lo, x1, fmaf(s_lo, q[1], a[1]));
+                a[2] = fmaf(b_hi, x0, fmaf(s_hi, q[2], a[2]));
+                a[3] = fmaf(b_hi, x1, fmaf(s_hi, q[3], a[3]));
+                q[0] = q[1] = q[2] = q[3] = 0.f;
+            }
+        }
+        mma_steps_exact<BITS, GROUP, NB, S + 1>(wl, wh, sl, sh, b, xs, c, acc, accg);
+    }
+}
+
 // The activation fragments of one block: 8 steps x (k low, k high) for each
 // 8-row activation block.  xa is this lane's ldmatrix row address in the tile.
 template <int NB>
@@ -190,7 +234,7 @@ __device__ __forceinline__ void segment_end(const DecParams& p, const DecProj& P
     if (lane == 0) *ctr = 0u;
 }
 
-template <int BITS, int GROUP, int NB>
+template <int BITS, int GROUP, int NB, bool EXACT>
 __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
     decode_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -228,17 +272,18 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
         sh->abort_flag = 0;
         fence_mbar_init();
     }
-    // Activation rows M..8NB-1 stay zero for the whole launch: the TMA loads
-    // write rows 0..M-1 only (the tensor map's box is M rows).
+    // Activation rows M..8NB-1 (and their group sums) stay zero for the whole
+    // launch: the producers write rows 0..M-1 only (the tensor map's box is M
+    // rows).
     for (int s = 0; s < NS; ++s)
-        for (uint32_t off = 16u * threadIdx.x; off < 2u * XT; off += 16u * D_THREADS)
+        for (uint32_t off = 16u * threadIdx.x; off < 2u * XT + 2u * D_XSUM; off += 16u * D_THREADS)
             sts_zero16(ring + (uint32_t)s * SLOT + 2u * BB + off);
     fence_proxy_async_smem();  // generic-proxy zeros -> TMA writes
     __syncthreads();
     volatile int* abort_flag = &sh->abort_flag;
     if (threadIdx.x == 0) pdl_launch_dependents();
 
-    if (warp == D_WPROD || warp == D_XPROD) {
+    if (warp == D_WPROD || (warp == D_XPROD && !EXACT)) {
         // ---------------------------------------------------------- producers
         // The weights never depend on an earlier kernel, so their producer
         // starts before the grid dependency is resolved; the activations may
@@ -271,6 +316,60 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
             if (*abort_flag)  // no copy may still be landing when the CTA exits
                 for (int j = max(0, issued - NS); j < issued; ++j) (void)mbar_wait(BAR(full, j % NS), (uint32_t)((j / NS) & 1));
         }
+    } else if (warp == D_XPROD) {
+        // ------------------------- activations and their group sums (exact-codes mode)
+        // The whole warp loads each block's M rows of x (lane l: k = 4l .. 4l + 3),
+        // stores them in the tile layout, and adds each group's values (the
+        // lanes of a group reduce in a fixed tree) into the slot's sums.
+        pdl_wait();  // x may come from the previous kernel
+        constexpr int LPG = GROUP / 4;  // lanes per group
+        for (int j = 0; j < npairs; ++j) {
+            const int s = j % NS;
+            int okw = 1;
+            if (lane == 0) okw = wait_or_abort_lazy(BAR(empty, s), (uint32_t)((j / NS) & 1) ^ 1u, abort_flag, p.status);
+            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+            const int nb2 = min(2, nblk - 2 * j);
+            const uint32_t st = ring + (uint32_t)s * SLOT;
+            // both blocks' loads first (one round trip to L2 per slot), then the stores and sums
+            uint32_t xw[2][8 * NB][2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t k0 = (int64_t)((u0 + 2 * j + h) % KB) * KBLK + 4 * lane;
+                const bool in = h < nb2 && k0 < p.K;  // K is a multiple of 32: a lane's four values are all in or out
+#pragma unroll
+                for (int m = 0; m < 8 * NB; ++m) {
+                    xw[h][m][0] = xw[h][m][1] = 0u;
+                    if (m < M && in) {
+                        const uint2 v = __ldg(reinterpret_cast<const uint2*>(p.x + (int64_t)m * p.K + k0));
+                        xw[h][m][0] = v.x;
+                        xw[h][m][1] = v.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (h >= nb2) break;
+                const uint32_t tile = st + 2u * BB + (uint32_t)h * XT;
+                const uint32_t sums = st + 2u * BB + 2u * XT + (uint32_t)h * D_XSUM;
+#pragma unroll
+                for (int m = 0; m < 8 * NB; ++m) {
+                    if (m >= M) break;
+                    asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(tile + (uint32_t)m * D_XROW + 8u * lane),
+                                 "r"(xw[h][m][0]), "r"(xw[h][m][1])
+                                 : "memory");
+                    float v = __uint_as_float(xw[h][m][0] << 16) + __uint_as_float(xw[h][m][0] & 0xFFFF0000u) +
+                              __uint_as_float(xw[h][m][1] << 16) + __uint_as_float(xw[h][m][1] & 0xFFFF0000u);
+#pragma unroll
+                    for (int off = 1; off < LPG; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                    if (lane % LPG == 0)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sums + (uint32_t)((lane / LPG) * 16 + m) * 4u),
+                                     "f"(v)
+                                     : "memory");
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(full, s));  // the tiles and sums are written
+        }
     } else {
         // ---------------------------------------------------------- consumers
         const int g = lane >> 2, c = lane & 3;
@@ -278,9 +377,9 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
         // ldmatrix: lanes 8j .. 8j + 7 address matrix j's eight rows; matrix j
         // of a pair of steps is (step 2p + j/2, k half j mod 2)
         const uint32_t xlane = (uint32_t)(lane & 7) * D_XROW + (uint32_t)((lane >> 3) & 1) * 16u + (uint32_t)(lane >> 4) * 32u;
-        float acc[4 * NB];
+        float acc[4 * NB], accg[4 * NB];  // accg: the current group's sum of q x (exact-codes mode)
 #pragma unroll
-        for (int e = 0; e < 4 * NB; ++e) acc[e] = 0.f;
+        for (int e = 0; e < 4 * NB; ++e) acc[e] = accg[e] = 0.f;
         pdl_wait();  // y, the partials and the counters may still be in use by the previous kernel
         int kb = u0 % KB, tile = u0 / KB, seg_start = u0;
         for (int j = 0; j < npairs; ++j) {
@@ -300,11 +399,19 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                 load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, r_hi), sh2);
                 uint32_t b[NB][8][2];
                 load_x_frags<NB>(st + 2u * BB + (uint32_t)h * XT + xlane, b);
-                if (h == 1 || !pair) {  // every read of the slot is issued: release it
+                if (!EXACT && (h == 1 || !pair)) {  // every read of the slot is issued: release it
                     __syncwarp();
                     if (lane == 0) mbar_arrive(BAR(empty, s));
                 }
-                mma_steps<BITS, GROUP, NB>(wl, wh, sl, sh2, b, acc);
+                if constexpr (EXACT)
+                    mma_steps_exact<BITS, GROUP, NB>(wl, wh, sl, sh2, b, st + 2u * BB + 2u * XT + (uint32_t)h * D_XSUM, c,
+                                                     acc, accg);
+                else
+                    mma_steps<BITS, GROUP, NB>(wl, wh, sl, sh2, b, acc);
+                if (EXACT && (h == 1 || !pair)) {  // the group sums are read too: release the slot
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(empty, s));
+                }
                 const int u = u0 + 2 * j + h;
                 if (kb == KB - 1 || u == u1 - 1) {  // this block ends a tile segment
                     segment_end<NB>(p, P, acc, tile, (seg_start == tile * KB) && (kb == KB - 1), seg_start == u0, cta,
@@ -326,40 +433,45 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
     __syncthreads();
 }
 
+template <int BITS, int GROUP, bool EXACT>
+cudaError_t launch_bge(const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
+    if (p.M > 8) return launch_pdl(decode_kernel<BITS, GROUP, 2, EXACT>, grid, D_THREADS, (size_t)D_SMEM, st, p, map);
+    return launch_pdl(decode_kernel<BITS, GROUP, 1, EXACT>, grid, D_THREADS, (size_t)D_SMEM, st, p, map);
+}
 template <int BITS, int GROUP>
-cudaError_t launch_bg(const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    if (p.M > 8) return launch_pdl(decode_kernel<BITS, GROUP, 2>, grid, D_THREADS, (size_t)D_SMEM, st, p, map);
-    return launch_pdl(decode_kernel<BITS, GROUP, 1>, grid, D_THREADS, (size_t)D_SMEM, st, p, map);
+cudaError_t launch_bg(const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st, bool exact) {
+    return exact ? launch_bge<BITS, GROUP, true>(p, map, grid, st) : launch_bge<BITS, GROUP, false>(p, map, grid, st);
 }
 
 template <int BITS>
-cudaError_t launch_b(int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    if (group == 32) return launch_bg<BITS, 32>(p, map, grid, st);
-    if (group == 64) return launch_bg<BITS, 64>(p, map, grid, st);
-    return launch_bg<BITS, 128>(p, map, grid, st);
+cudaError_t launch_b(int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st, bool exact) {
+    if (group == 32) return launch_bg<BITS, 32>(p, map, grid, st, exact);
+    if (group == 64) return launch_bg<BITS, 64>(p, map, grid, st, exact);
+    return launch_bg<BITS, 128>(p, map, grid, st, exact);
 }
 
 // The kernel's shared-memory limit, the largest shared-memory carveout (two
 // CTAs of 110 KB per SM), and how many CTAs of it an SM holds (min over the
 // instantiations, which differ only in registers).
-template <int BITS, int GROUP, int NB>
+template <int BITS, int GROUP, int NB, bool EXACT>
 cudaError_t allow_bgn(int* per_sm) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<BITS, GROUP, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)D_SMEM);
+    auto* k = decode_kernel<BITS, GROUP, NB, EXACT>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)D_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<BITS, GROUP, NB>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS, GROUP, NB>, D_THREADS, (size_t)D_SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, D_THREADS, (size_t)D_SMEM);
     if (e != cudaSuccess) return e;
     *per_sm = min(*per_sm, n);
     return cudaSuccess;
 }
 template <int BITS, int GROUP>
 cudaError_t allow_bg(int* per_sm) {
-    cudaError_t e = allow_bgn<BITS, GROUP, 1>(per_sm);
-    return e != cudaSuccess ? e : allow_bgn<BITS, GROUP, 2>(per_sm);
+    for (cudaError_t e : {allow_bgn<BITS, GROUP, 1, false>(per_sm), allow_bgn<BITS, GROUP, 2, false>(per_sm),
+                          allow_bgn<BITS, GROUP, 1, true>(per_sm), allow_bgn<BITS, GROUP, 2, true>(per_sm)})
+        if (e != cudaSuccess) return e;
+    return cudaSuccess;
 }
 
 template <int BITS>
@@ -381,14 +493,14 @@ cudaError_t decode_allow_smem(int* ctas_per_sm) {
 }
 
 cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool exact) {
     switch (bits) {
-        case 2: return launch_b<2>(group, p, map, grid, st);
-        case 3: return launch_b<3>(group, p, map, grid, st);
-        case 4: return launch_b<4>(group, p, map, grid, st);
-        case 5: return launch_b<5>(group, p, map, grid, st);
-        case 6: return launch_b<6>(group, p, map, grid, st);
-        case 8: return launch_b<8>(group, p, map, grid, st);
+        case 2: return launch_b<2>(group, p, map, grid, st, exact);
+        case 3: return launch_b<3>(group, p, map, grid, st, exact);
+        case 4: return launch_b<4>(group, p, map, grid, st, exact);
+        case 5: return launch_b<5>(group, p, map, grid, st, exact);
+        case 6: return launch_b<6>(group, p, map, grid, st, exact);
+        case 8: return launch_b<8>(group, p, map, grid, st, exact);
         default: return cudaErrorInvalidValue;
     }
 }

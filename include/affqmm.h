@@ -137,6 +137,18 @@ AFFQMM_API int affqmm_workspace_bytes_stacked(int count, const affqmm_weight* ws
 AFFQMM_API int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y,
                void* workspace, size_t ws_bytes, void* stream);
 
+/* The exact-codes form of the projection for M <= 16 activation rows -- the
+ * pages' lane projection ("Gemma 4 12B on the native Metal engine" page, the
+ * reg-variant commit: codes kept exact, group sums of x precomputed):
+ *     y[m, n] = bf16( sum_g ( s_g * sum_{k in g} q[n,k] x[m,k]
+ *                             + b_g * sum_{k in g} x[m,k] ) ),   fp32 sums
+ * The weights are never rounded to bf16, so the result differs from
+ * affqmm_run by the rounding of bf16(s * q + b).  Arguments, workspace and
+ * errors as affqmm_run, except that M > 16 is refused with E_M.  Same inputs,
+ * same bits. */
+AFFQMM_API int affqmm_run_exact(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y, void* workspace,
+                                size_t ws_bytes, void* stream);
+
 /* Several projections of the same x in one launch (q/k/v, gate/up stacks).
  *   ws      host array of `count` weight views (1 <= count <= AFFQMM_MAX_STACK)
  *           with equal K, bits and group

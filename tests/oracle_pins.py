@@ -329,6 +329,29 @@ def pin_group_sum_identity(orc, seed=17):
         assert np.max(dev / mag) > 0
 
 
+def pin_qmm_groupsum_bruteforce(orc, seed=23):
+    """The exact-codes form against exact rational arithmetic on tiny shapes:
+    y_gs = sum_g (s_g * sum_{k in g} q_k x_k + b_g * sum_{k in g} x_k), with the
+    codes exact (no bf16 rounding of the weights); and mag = sum |s q + b| |x|."""
+    rng = np.random.default_rng(seed)
+    for bits, group, M, N, K in [(4, 64, 2, 3, 128), (3, 32, 1, 2, 96), (8, 128, 1, 2, 256), (6, 32, 2, 2, 64)]:
+        x, codes, s, b = _small_problem(rng, bits, group, M, N, K)
+        y_gs, mag = orc.qmm_groupsum(bits, group, x, codes, s, b)
+        G = K // group
+        for m in range(M):
+            for n in range(N):
+                exact = Fraction(0)
+                amag = Fraction(0)
+                for j in range(G):
+                    sv, bv = bf16_value(int(s[n, j])), bf16_value(int(b[n, j]))
+                    xs = [bf16_value(int(v)) for v in x[m, j * group:(j + 1) * group]]
+                    qs = [int(q) for q in codes[n, j * group:(j + 1) * group]]
+                    exact += sv * sum((q * xv for q, xv in zip(qs, xs)), Fraction(0)) + bv * sum(xs, Fraction(0))
+                    amag += sum((abs(sv * q + bv) * abs(xv) for q, xv in zip(qs, xs)), Fraction(0))
+                assert abs(Fraction(float(y_gs[m, n])) - exact) <= amag * Fraction(1, 2 ** 44), (bits, group, m, n)
+                assert abs(Fraction(float(mag[m, n])) - amag) <= amag * Fraction(1, 2 ** 44), (bits, group, m, n)
+
+
 def _embed_exact_bits(orc_w_bits: int, scale_bits: int) -> int:
     """bf16(w * scale) from the exact product (w, scale finite bf16 patterns)."""
     w, sc = bf16_value(orc_w_bits), bf16_value(scale_bits)
@@ -383,6 +406,7 @@ ALL_PINS = [
     pin_one_hot_rows,
     pin_constant_code_groups,
     pin_group_sum_identity,
+    pin_qmm_groupsum_bruteforce,
     pin_embed_rows_exact,
     pin_embed_rows_special_cases,
 ]

@@ -114,6 +114,19 @@ def test_run_host_refusals_before_anything_is_enqueued(L):
     assert run_host(ctypes.byref(w), M=0) == 0
 
 
+def test_run_exact_refusals_before_any_launch(L):
+    names = api.STATUS_NAMES
+    w = _w()
+    run = lambda wp, M=1, x=0x200000, y=0x300000: L.affqmm_run_exact(wp, x, M, y, None, 0, None)
+    assert names[run(None)] == "AFFQMM_E_NULL"
+    assert names[run(ctypes.byref(_w(group=48)))] == "AFFQMM_E_GROUP"
+    assert names[run(ctypes.byref(w), M=17)] == "AFFQMM_E_M"   # the exact-codes form is the decode path only
+    assert names[run(ctypes.byref(w), M=-1)] == "AFFQMM_E_M"
+    assert names[run(ctypes.byref(w), x=0)] == "AFFQMM_E_NULL"
+    assert names[run(ctypes.byref(w), y=0x300001)] == "AFFQMM_E_ALIGN"
+    assert run(ctypes.byref(w), M=0) == 0
+
+
 def test_stacked_refusals(L):
     names = api.STATUS_NAMES
     arr = (api.CWeight * 2)(_w(), _w(K=512))
