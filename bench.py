@@ -107,9 +107,15 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def source_digest() -> str:
+SHARED_KERNEL_HEADERS = KERNEL_SOURCES[3:]
+
+
+def source_digest(kernel: str | None = None) -> str:
+    """Hash of the kernel sources: of one kernel ("decode", "prompt", "embed":
+    its .cu and the shared device headers), or of all of them."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    rels = KERNEL_SOURCES if kernel is None else [f"group_affine_bit_gb300/csrc/{kernel}.cu", *SHARED_KERNEL_HEADERS]
+    for rel in rels:
         p = os.path.join(ROOT, rel)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
@@ -132,7 +138,7 @@ def committed_traffic(key: str):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(key)
-    if not d or d.get("src_digest") != source_digest():
+    if not d or d.get("src_digest") != source_digest(key.split()[0]):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -299,7 +305,9 @@ class Workload:
             return dict(kernel=f"prompt_kernel<{c0.bits},{c0.group}>", bound="tensor",
                         units_per_step=float(sum(c.flops for c in self.cases)), unit="TFLOP/s",
                         traffic_key=f"prompt {self.name}")
-        return dict(kernel=f"decode_kernel<{c0.bits},{c0.group}>", bound="hbm",
+        nb = 2 if max(c.M for c in self.cases) > 8 else 1
+        exact = "true" if getattr(c0, "exact", False) else "false"
+        return dict(kernel=f"decode_kernel<{c0.bits},{c0.group},{nb},{exact}>", bound="hbm",
                     units_per_step=float(sum(c.algorithmic_bytes for c in self.cases)), unit="GB/s",
                     traffic_key=f"decode {self.name}")
 
