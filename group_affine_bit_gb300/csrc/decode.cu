@@ -12,18 +12,24 @@
 // multiply-adds of 16 rows x 16 k for up to 8 activation rows, where fp32
 // FMAs on the CUDA cores would cost one instruction per weight and row.
 //
-// Per CTA (two per SM):
-//   * one producer thread streams the run's blocks (9 KB at 4 bits, group
-//     64) two at a time with 1-D bulk copies into a ring of weight slots, and
-//     another loads each block's activation tile -- M rows x 136 k, 272 bytes
-//     a row so that the eight rows of a matrix load sit on distinct banks --
-//     with TMA into a ring of tiles whose rows M..15 stay zero;
+// Per CTA (two per SM), one ring of slots, each holding two consecutive
+// blocks of the run (9 KB each at 4 bits, group 64) and their two activation
+// tiles:
+//   * one producer thread fills a slot's blocks with one 1-D bulk copy, and
+//     another loads the slot's activation tiles -- M rows x 136 k, 272 bytes a
+//     row so that the eight rows of a matrix load sit on distinct banks --
+//     with TMA into tiles whose rows M..15 stay zero;
 //   * eight consumer warps each own 16 rows of every block: thread t (group
 //     g = t/4, class c = t mod 4) reads class c's code words of rows g and
-//     g + 8 and the rows' scale/bias words (affqmm_format.cuh), releases the
-//     slot, loads the activation fragments with ldmatrix, and for each of the
-//     8 16-deep steps rounds four weight pairs -- bf16(fma(s, q, b)), one
-//     rounding -- and issues one mma (two when M > 8) into fp32 registers.
+//     g + 8 and the rows' scale/bias words (affqmm_format.cuh), loads the
+//     activation fragments with ldmatrix, releases the slot after its last
+//     read, and for each of the 8 16-deep steps rounds four weight pairs --
+//     bf16(fma(s, q, b)), one rounding -- and issues one mma (two when M > 8)
+//     into fp32 registers.
+// The exact-codes instantiation (the pages' lane projection) puts the exact
+// codes into the A fragments and adds s * sum(q x) + b * sum(x) per group;
+// its activation warp loads the tiles itself and writes each group's sum of
+// x next to them.
 // Work split ("stream-K"): the projection's blocks, numbered tile-major, are
 // cut into one contiguous run per CTA.  A tile cut by run boundaries gets one
 // fp32 partial per run; the last warp to arrive (an atomic counter per tile
