@@ -64,3 +64,14 @@ def test_reference_arm_prints_on_rank_zero_only(rank, prints):
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_times_the_exact_codes_oracle_for_the_exact_workload():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "gate_up_exact", "--steps", "1", "--warmup", "1", "--cpu-seconds", "0.2"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.strip()][0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "gate_up_exact"
+    assert "exact-codes oracle" in d["cpu_baseline"]["sample"] and d["cpu_baseline"]["cores"] == 1
