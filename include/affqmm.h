@@ -208,7 +208,7 @@ AFFQMM_API int affqmm_workspace_status(void* workspace, void* stream);
 #define AFFQMM_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* affqmm_run for M <= 16 activation rows without any device memory from the
- * caller beyond x and y.  The paper has no counterpart to this entry point:
+ * caller beyond x and y.  The method's pages have no counterpart to this entry point:
  * it is a convenience of this library.
  *
  * Who needs it: code that runs where it cannot allocate device memory -- a
