@@ -64,6 +64,11 @@ PLANTS = {
         "uint16_t w = has_scale ? oracle_dequant_one(q, oracle_bf16_from_double(oracle_bf16_to_double(scales[n * G + j]) * sc), "
         "oracle_bf16_from_double(oracle_bf16_to_double(biases[n * G + j]) * sc)) : "
         "oracle_dequant_one(q, scales[n * G + j], biases[n * G + j]); if (has_scale) { out[t * K + k] = w; continue; }"),
+    # exact-codes form: the bias times the group's sum of x is dropped
+    "groupsum_bias_dropped": ("acc += s * sqx + b * sx;", "acc += s * sqx;"),
+    # exact-codes form: the codes' products use the next row's codes
+    "groupsum_wrong_code_row": ("double q = (double)codes[n * K + k];",
+                                "double q = (double)codes[((n + 1) % N) * K + k];"),
     # the scale and bias patterns swapped
     "swapped_scale_bias": ("double sd = oracle_bf16_to_double(s);\n    double bd = oracle_bf16_to_double(b);",
                            "double sd = oracle_bf16_to_double(b);\n    double bd = oracle_bf16_to_double(s);"),
