@@ -62,6 +62,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="no nvidia-smi sampling (for runs under a profiler)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     return ap.parse_args(argv)
 
@@ -731,7 +732,7 @@ def main(argv=None):
     steps = args.steps if args.steps is not None else wl.default_steps
     warmup = max(3, args.warmup)
 
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
     if sampler:
         sampler.start()
     seconds, graphs = time_steps(wl, steps, warmup, dist, device)

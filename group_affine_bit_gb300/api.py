@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "affqmm_run_host": (i32, [wp, vp, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]),
             "affqmm_run_exact": (i32, [wp, vp, i64, vp, vp, ctypes.c_size_t, vp]),
             "affqmm_embed_rows": (i32, [wp, vp, i64, i32, ctypes.c_uint16, vp, vp, vp]),
+            "affqmm_test_fault_wait": (i32, [i64]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -289,8 +290,16 @@ def dequant(w: PackedWeight, stream=None) -> torch.Tensor:
 
 
 def workspace_status(buf: torch.Tensor, stream=None) -> int:
-    """Read and clear a workspace's device status word (0 = ok)."""
+    """Read a workspace's device status word (0 = ok; after a timeout the
+    library zeroes the status word and the merge counters again)."""
     return int(lib().affqmm_workspace_status(buf.data_ptr(), _stream_ptr(stream)))
+
+
+def test_fault_wait(cycles: int) -> None:
+    """Test hook: while cycles > 0, decode launches (M <= 16) first wait, at
+    most `cycles` SM clock cycles, on a barrier nothing completes, so the
+    bounded wait runs out and the workspace status reports a timeout."""
+    _check(lib().affqmm_test_fault_wait(int(cycles)), "affqmm_test_fault_wait")
 
 
 def run_noalloc(w: PackedWeight, x: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Tensor:

@@ -90,6 +90,7 @@ int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, De
     p.KB = KB;
     p.K = K;
     p.M = (int32_t)M;
+    p.fault_wait = decode_fault_wait();
     const int64_t resident = (int64_t)d.sms * d.dec_ctas_per_sm;
     int64_t ctas = 0, tiles_total = 0;
     for (int i = 0; i < count; ++i) {
@@ -497,10 +498,17 @@ int affqmm_workspace_status(void* workspace, void* stream) {
     if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess) return AFFQMM_E_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return AFFQMM_E_CUDA;
     if (word == 0) return AFFQMM_OK;
-    const uint32_t zero = 0;
-    if (cudaMemcpyAsync(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice, st) != cudaSuccess) return AFFQMM_E_CUDA;
+    // A kernel that gave up may have left merge counters behind as well:
+    // clear the status word and every counter, the workspace's zeroed prefix.
+    if (cudaMemsetAsync(workspace, 0, AFFQMM_WORKSPACE_ZEROED, st) != cudaSuccess) return AFFQMM_E_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return AFFQMM_E_CUDA;
     return AFFQMM_E_TIMEOUT;
+}
+
+int affqmm_test_fault_wait(int64_t cycles) {
+    if (cycles < 0) return AFFQMM_E_ARG;
+    decode_set_fault_wait(cycles);
+    return AFFQMM_OK;
 }
 
 }  // extern "C"
@@ -522,25 +530,31 @@ namespace {
 // In host code `g_noalloc_scratch` names a host-side stand-in, not device
 // memory: kernels get the address that cudaGetSymbolAddress returns for the
 // current device, looked up once per device.
+// Only a successful lookup is kept: a failed one (for instance, one made
+// while the stream was being captured) is tried again on the next call.
 struct NoallocScratch {
     void* ptr = nullptr;
     bool ok = false;
 };
 NoallocScratch g_noalloc[kMaxDevices];
-std::once_flag g_noalloc_once[kMaxDevices];
+std::mutex g_noalloc_mutex;
 
 int noalloc_scratch(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return AFFQMM_E_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return AFFQMM_E_DEVICE;
-    std::call_once(g_noalloc_once[dev], [dev] {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoallocScratch& e = g_noalloc[dev];
+    if (!e.ok) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return;
-        g_noalloc[dev].ptr = p;
-        g_noalloc[dev].ok = true;
-    });
-    if (!g_noalloc[dev].ok) return AFFQMM_E_CUDA;
-    *out = g_noalloc[dev].ptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();  // leave no sticky error behind for the caller's next call
+            return AFFQMM_E_CUDA;
+        }
+        e.ptr = p;
+        e.ok = true;
+    }
+    *out = e.ptr;
     return AFFQMM_OK;
 }
 

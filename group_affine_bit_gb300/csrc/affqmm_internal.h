@@ -39,6 +39,7 @@ struct DecParams {
     uint32_t* status;        // device status word (bit 0: a bounded wait gave up)
     uint32_t* counters;
     float* partials;         // slot = 128 rows x 16 floats
+    int64_t fault_wait;      // test hook (0 = off): cycles the consumers wait on a barrier nothing completes
 };
 
 constexpr size_t kDecSlotFloats = 128 * 16;
@@ -109,6 +110,9 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, int threads, size_t
 // swizzle.  decode_allow_smem sets the kernels' shared-memory attributes and
 // reports how many decode CTAs one SM holds.
 cudaError_t decode_allow_smem(int* ctas_per_sm);
+// The decode launches' fault_wait test hook (affqmm_test_fault_wait).
+int64_t decode_fault_wait();
+void decode_set_fault_wait(int64_t cycles);
 cudaError_t launch_decode(int bits, int group, const DecParams& p, const CUtensorMap& map, int grid, cudaStream_t st,
                           bool exact = false);
 // prompt.cu: the tensor map describes x [M, K] bf16 with a 64 x 128 box.

@@ -126,8 +126,8 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* addr, unsigned v)
 // A suspended try_wait also returns (false) when another thread arrives on
 // the barrier without completing the phase, so the abort flag and the clock
 // are looked at only every eighth return: those early wake-ups stay cheap.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t* status) {
+__device__ __forceinline__ bool wait_or_abort_within(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                     uint32_t* status, long long limit_cycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
@@ -135,12 +135,16 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
         for (int r = 0; r < 8; ++r)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit_cycles) {
             *abort_flag = 1;
             atomicOr(status, 1u);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* status) {
+    return wait_or_abort_within(bar, parity, abort_flag, status, kWaitLimitCycles);
 }
 
 // The same for threads that are not on the critical path (the producers,

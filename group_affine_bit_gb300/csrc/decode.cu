@@ -71,6 +71,8 @@ constexpr uint32_t D_RING0 = 1024u;           // the ring starts here; the barri
 struct DecSmem {
     uint64_t full[D_SLOTS_MAX];
     uint64_t empty[D_SLOTS_MAX];
+    uint64_t never;      // completed by nothing: the fault_wait test hook waits on it
+    int issued[2];       // slots armed by the weights producer [0] and the activation producer [1]
     int abort_flag;
 };
 static_assert(sizeof(DecSmem) <= D_RING0, "barriers fit below the ring");
@@ -207,15 +209,16 @@ __device__ __forceinline__ void segment_end(const DecParams& p, const DecProj& P
         const int r = (e & 2) ? r_hi : r_lo;
         if (m < M) __stcg(sp + r * 16 + m, acc[e]);
     }
+    __threadfence();  // every lane's partial is visible GPU-wide before the arrival
     __syncwarp();
     unsigned prev = 0;
     unsigned* ctr = &p.counters[(size_t)(P.ctr_begin + tile) * D_CWARPS + warp];
     if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
     prev = __shfl_sync(0xffffffffu, prev, 0);
-    __syncwarp();
     const int t0 = tile * KB, t1 = t0 + KB - 1;
     const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
     if (prev != (unsigned)(cl - cf)) return;
+    __threadfence();  // the last arrival: every lane reads the other runs' partials after it
     float sum[4 * NB];
 #pragma unroll
     for (int e = 0; e < 4 * NB; ++e) sum[e] = 0.f;
@@ -275,6 +278,8 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
             mbar_init(BAR(full, s), 2);          // both producers
             mbar_init(BAR(empty, s), D_CWARPS);  // every consumer warp
         }
+        mbar_init(BAR(never, 0), 1);
+        sh->issued[0] = sh->issued[1] = 0;
         sh->abort_flag = 0;
         fence_mbar_init();
     }
@@ -319,8 +324,7 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                 }
                 issued = j + 1;
             }
-            if (*abort_flag)  // no copy may still be landing when the CTA exits
-                for (int j = max(0, issued - NS); j < issued; ++j) (void)mbar_wait(BAR(full, j % NS), (uint32_t)((j / NS) & 1));
+            sh->issued[wprod ? 0 : 1] = issued;
         }
     } else if (warp == D_XPROD) {
         // ------------------------- activations and their group sums (exact-codes mode)
@@ -374,7 +378,10 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(full, s));  // the tiles and sums are written
+            if (lane == 0) {
+                mbar_arrive(BAR(full, s));  // the tiles and sums are written
+                sh->issued[1] = j + 1;
+            }
         }
     } else {
         // ---------------------------------------------------------- consumers
@@ -387,8 +394,14 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
 #pragma unroll
         for (int e = 0; e < 4 * NB; ++e) acc[e] = accg[e] = 0.f;
         pdl_wait();  // y, the partials and the counters may still be in use by the previous kernel
+        // Test hook: wait, bounded by p.fault_wait cycles, on a barrier that
+        // nothing completes; the wait runs out, sets the status word and the
+        // abort flag, and the CTA finishes without output.
+        const bool run = p.fault_wait <= 0 ||
+                         __all_sync(0xffffffffu, wait_or_abort_within(BAR(never, 0), 0u, abort_flag, p.status,
+                                                                      p.fault_wait));
         int kb = u0 % KB, tile = u0 / KB, seg_start = u0;
-        for (int j = 0; j < npairs; ++j) {
+        for (int j = 0; run && j < npairs; ++j) {
             const int s = j % NS;
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), (uint32_t)((j / NS) & 1), abort_flag, p.status)))
                 break;
@@ -433,10 +446,20 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
             }
         }
     }
-#undef BAR
-    // teardown: every role has left its loop; after an abort the producers
-    // have waited for the copies they issued
+    // teardown: every role has left its loop.  After an abort, no copy may
+    // still be landing when the CTA exits: one thread waits for each slot a
+    // producer armed, making the arrival the other producer never made (a
+    // slot's phase needs both), so every wait ends once the bytes are in.
     __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        const int iw = sh->issued[0], ix = sh->issued[1];
+        const int hi = max(iw, ix), lo = min(iw, ix);
+        for (int j = max(0, hi - NS); j < hi; ++j) {
+            if (j >= lo) mbar_arrive(BAR(full, j % NS));
+            (void)mbar_wait(BAR(full, j % NS), (uint32_t)((j / NS) & 1));
+        }
+    }
+#undef BAR
 }
 
 template <int BITS, int GROUP, bool EXACT>
@@ -488,6 +511,12 @@ cudaError_t allow_b(int* per_sm) {
 }
 
 }  // namespace
+
+static long long g_fault_wait = 0;  // affqmm_test_fault_wait
+
+int64_t decode_fault_wait() { return __atomic_load_n(&g_fault_wait, __ATOMIC_RELAXED); }
+
+void decode_set_fault_wait(int64_t cycles) { __atomic_store_n(&g_fault_wait, (long long)cycles, __ATOMIC_RELAXED); }
 
 cudaError_t decode_allow_smem(int* ctas_per_sm) {
     int n = D_CTAS_PER_SM;

@@ -59,6 +59,11 @@ __global__ void __launch_bounds__(TILE_N) pack_kernel(int group, int64_t N, int6
         }
         sb[gi] = v;
     }
+    // The run kernels start copying packed weights before they wait on the
+    // kernel ahead of them in the stream (programmatic dependent launch): make
+    // this thread's writes visible GPU-wide before the block exits, which is
+    // when this kernel (it never triggers early) lets a dependent start.
+    __threadfence();
 }
 
 // One CTA per block, one thread per row: the run kernels' loads and

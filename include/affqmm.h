@@ -26,12 +26,16 @@
  *     `stream` (a cudaStream_t; NULL means the legacy default stream) and is
  *     asynchronous: the call returns once the launches are queued.
  *   - The caller allocates and owns every buffer; the library never
- *     allocates device memory and keeps no state between calls.  The one
- *     exception is affqmm_run_noalloc, which works in a fixed scratch array
- *     that the library's module places in device memory (see there).
+ *     allocates device memory and keeps no state between calls.  The
+ *     exceptions: affqmm_run_noalloc works in a fixed scratch array that the
+ *     library's module places in device memory (see there), and the test
+ *     hook affqmm_test_fault_wait sets a process-wide switch.
  *   - Every argument is validated on the host before anything is launched.
- *     A rejected call returns a nonzero affqmm_status and launches nothing.
- *     Nothing is thrown or aborted across the ABI.
+ *     A rejected call returns a nonzero affqmm_status, which names the reason
+ *     (affqmm_strerror), and launches nothing -- refusals by name, as the
+ *     pages' engines refuse what they do not serve ("Gemma 4 12B on the
+ *     native Metal engine" page, the serving commit that refuses unsupported
+ *     options by name).  Nothing is thrown or aborted across the ABI.
  *   - bf16 values travel as uint16_t bit patterns.
  */
 #ifndef AFFQMM_H
@@ -92,30 +96,51 @@ AFFQMM_API const char* affqmm_strerror(int status);
 AFFQMM_API int affqmm_version(void);
 
 /* Bytes of packed storage for an N x K table (host call, no GPU needed).
+ * The table is MLX's affine one -- codes of 2, 3, 4, 5, 6 or 8 bits with a
+ * bf16 scale and bias per group of 32, 64 or 128 along a row ("cuda gemma4:
+ * images on the 12B" page, the embed_rows commit) -- stored in this
+ * library's own aligned blocks, as the "Gemma 4 12B on the native Metal
+ * engine" page copies each linear's tensors to aligned storage for the
+ * projection's word reads (its commit on aligned copies of the MLX tensors).
  * Rows are padded to multiples of 128 and the depth to multiples of 128; the
- * padding holds zero codes with zero scale and bias.
+ * padding holds zero codes with zero scale and bias.  When N and K are
+ * multiples of 128 the size is N*K*bits/8 + 4*N*K/group bytes: the codes and
+ * one scale and one bias per group, nothing more.
  * Errors: E_NULL (bytes), E_BITS, E_GROUP, E_SHAPE. */
 AFFQMM_API int affqmm_packed_bytes(int bits, int group, int64_t N, int64_t K, size_t* bytes);
 
-/* Pack a canonical affine table into the library's layout.
+/* Pack a canonical affine table into the library's layout (the table of the
+ * embed_rows commit of the "cuda gemma4: images on the 12B" page: MLX's
+ * affine tables at 2/3/4/5/6/8 bits, groups of 32/64/128; copied into
+ * aligned blocks as the Metal page's aligned-copies commit does for the
+ * projection's u32 word reads).
  *   codes   device, uint8 [N, K] row-major, one code per byte; bits above
  *           `bits` are ignored (a code is taken modulo 2^bits)
  *   scales  device, bf16 [N, K/group] row-major
  *   biases  device, bf16 [N, K/group] row-major
  *   packed  device, affqmm_packed_bytes() bytes, 256-byte aligned, written
  * The same table as MLX's affine quantization stores it (scale and bias per
- * group along a row), unpacked to one code per byte.
+ * group along a row), unpacked to one code per byte.  The packing kernel
+ * makes its writes visible device-wide before it finishes, so a run call
+ * enqueued right after it on the same stream reads the new weights (see
+ * affqmm_run on weights written by the preceding kernel).
  * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_CUDA. */
 AFFQMM_API int affqmm_pack(int bits, int group, int64_t N, int64_t K,
                 const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
                 void* packed, void* stream);
 
 /* Bytes of workspace that affqmm_run needs for this weight and M on the
- * current device (split-K partial sums, merge counters and a status word).
+ * current device: a status word, merge counters and the fp32 partial sums of
+ * the depth split, which the pages' lane projection also makes ("Gemma 4 12B
+ * on the native Metal engine" page, the per-shape K-split commit: o and down
+ * split 4 ways, gate/up and the head 8); here the split is cut evenly over
+ * the device's SMs and its partials are added in a fixed order.  0 when the
+ * call needs none.
  * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_M, E_DEVICE, E_CUDA. */
 AFFQMM_API int affqmm_workspace_bytes(const affqmm_weight* w, int64_t M, size_t* bytes);
 
-/* The same for a stacked call over `count` weights. */
+/* The same for a stacked call (affqmm_run_stacked) over the `count` weights
+ * of the host array `ws`. */
 AFFQMM_API int affqmm_workspace_bytes_stacked(int count, const affqmm_weight* ws, int64_t M,
                                    size_t* bytes);
 
@@ -132,6 +157,15 @@ AFFQMM_API int affqmm_workspace_bytes_stacked(int count, const affqmm_weight* ws
  *              reported AFFQMM_E_TIMEOUT, zero that prefix again.
  * M = 0 or N = 0 launches nothing; K = 0 writes zeros.
  * The result is deterministic: the same inputs give the same bits.
+ * Ordering: the kernels are launched with programmatic dependent launch.
+ * They read x, and write y and the workspace, only after waiting for the
+ * kernel ahead of them in the stream, but they start copying the packed
+ * weights before that wait.  So the packed weights must be complete when the
+ * preceding kernel on `stream` lets its dependents start: affqmm_pack
+ * guarantees it; a caller's own kernel that writes packed weights must fence
+ * its writes device-wide (__threadfence) before it finishes and must not
+ * trigger its dependents early, or the two must be separated by an event
+ * wait or a stream synchronization.
  * Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_M, E_WORKSPACE,
  *         E_DEVICE, E_CUDA. */
 AFFQMM_API int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y,
@@ -149,11 +183,17 @@ AFFQMM_API int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, 
 AFFQMM_API int affqmm_run_exact(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y, void* workspace,
                                 size_t ws_bytes, void* stream);
 
-/* Several projections of the same x in one launch (q/k/v, gate/up stacks).
+/* Several projections of the same x in one launch: a layer's q/k/v or
+ * gate/up stack ("Gemma 4 12B on the native Metal engine" page, the commit
+ * that packs each layer's q/k/v, o, gate/up and down stacks and the tied
+ * head once: seven shapes).
  *   ws      host array of `count` weight views (1 <= count <= AFFQMM_MAX_STACK)
- *           with equal K, bits and group
+ *           with equal K, bits and group, passed by value in one array (the
+ *           views are small structs; an array of them is what the caller
+ *           builds once per layer)
  *   ys      host array of `count` device pointers, ys[i] is bf16 [M, ws[i].N]
- * Each ys[i] equals affqmm_run(&ws[i], x, ...) bit for bit.
+ * Each ys[i] equals affqmm_run(&ws[i], x, ...) bit for bit.  Workspace and
+ * ordering as affqmm_run, sized by affqmm_workspace_bytes_stacked.
  * Errors: as affqmm_run, plus E_ARG for a bad count or mismatched weights. */
 AFFQMM_API int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M,
                        uint16_t* const* ys, void* workspace, size_t ws_bytes, void* stream);
@@ -198,10 +238,23 @@ AFFQMM_API int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* str
 AFFQMM_API int affqmm_embed_rows(const affqmm_weight* w, const int32_t* ids, int64_t T, int has_scale,
                                  uint16_t scale, uint16_t* out, uint32_t* status, void* stream);
 
-/* Read and clear the device status word of a workspace (synchronizes
- * `stream`).  Returns AFFQMM_OK, or AFFQMM_E_TIMEOUT when a kernel that used
- * this workspace gave up a bounded wait (its outputs are then invalid). */
+/* Read the device status word of a workspace that run calls used
+ * (synchronizes `stream`).  Returns AFFQMM_OK, or AFFQMM_E_TIMEOUT when a
+ * kernel that used this workspace gave up a bounded wait (its outputs are
+ * then invalid); in that case the whole AFFQMM_WORKSPACE_ZEROED prefix
+ * (status word and merge counters) is zeroed again, so the workspace serves
+ * the next call as it is. */
 AFFQMM_API int affqmm_workspace_status(void* workspace, void* stream);
+
+/* Test hook for the timeout path (no counterpart on the pages): while
+ * `cycles` > 0, every decode launch (M <= 16) that this process makes
+ * afterwards first has its consumer warps wait, at most `cycles` SM clock
+ * cycles, on a barrier that nothing completes.  The wait runs out; the launch
+ * sets its workspace status word (affqmm_workspace_status then returns
+ * AFFQMM_E_TIMEOUT), writes no output, waits for the copies it started and
+ * exits.  0 restores normal launches.  Not for production use.
+ * Errors: E_ARG (cycles < 0). */
+AFFQMM_API int affqmm_test_fault_wait(int64_t cycles);
 
 /* Largest M affqmm_run_noalloc takes, and the size of its built-in scratch. */
 #define AFFQMM_NOALLOC_MAX_M 16

@@ -117,7 +117,10 @@ class Oracle:
             raise ValueError(f"oracle_qmm rejected its arguments (rc={rc})")
         return y
 
-    def qmm_groupsum(self, bits, group, x, codes, scales, biases):
+    def qmm_groupsum(self, bits, group, x, codes, scales, biases, nthreads: int = 1):
+        """The exact-codes form.  nthreads > 1 splits the output rows n into
+        contiguous slices, one C call per slice from a thread pool (ctypes
+        releases the GIL); every output is the same single C computation."""
         x = np.ascontiguousarray(x, dtype=np.uint16)
         codes = np.ascontiguousarray(codes, dtype=np.uint8)
         scales = np.ascontiguousarray(scales, dtype=np.uint16)
@@ -126,11 +129,26 @@ class Oracle:
         N = codes.shape[0]
         y = np.empty((M, N), dtype=np.float64)
         mag = np.empty((M, N), dtype=np.float64)
-        rc = self.lib.oracle_qmm_groupsum(bits, group, M, N, K, _ptr(x, _u16p), _ptr(codes, _u8p),
-                                          _ptr(scales, _u16p), _ptr(biases, _u16p),
-                                          _ptr(y, _f64p), _ptr(mag, _f64p))
-        if rc:
-            raise ValueError(f"oracle_qmm_groupsum rejected its arguments (rc={rc})")
+
+        def rows(n0, n1):
+            yy = np.empty((M, n1 - n0), dtype=np.float64)
+            mm = np.empty((M, n1 - n0), dtype=np.float64)
+            rc = self.lib.oracle_qmm_groupsum(bits, group, M, n1 - n0, K, _ptr(x, _u16p),
+                                              _ptr(codes[n0:n1], _u8p), _ptr(scales[n0:n1], _u16p),
+                                              _ptr(biases[n0:n1], _u16p), _ptr(yy, _f64p), _ptr(mm, _f64p))
+            if rc:
+                raise ValueError(f"oracle_qmm_groupsum rejected its arguments (rc={rc})")
+            y[:, n0:n1] = yy
+            mag[:, n0:n1] = mm
+
+        nthreads = max(1, min(int(nthreads), N))
+        if nthreads == 1:
+            rows(0, N)
+        else:
+            from concurrent.futures import ThreadPoolExecutor
+            cuts = [N * t // nthreads for t in range(nthreads + 1)]
+            with ThreadPoolExecutor(nthreads) as ex:
+                list(ex.map(lambda t: rows(cuts[t], cuts[t + 1]), range(nthreads)))
         return y, mag
 
     # -- scaled embedding rows -------------------------------------------------

@@ -33,3 +33,25 @@ def assert_within_tolerance(y_gpu: torch.Tensor, y_ref: np.ndarray, what=""):
     ok, worst, bad = tolerance_report(u16(y_gpu), y_ref)
     assert ok, f"{what}: {bad} outputs outside 2^-7|y|+1e-3 rms (worst {worst:.3f} of the bound)"
     return worst
+
+
+# ----------------------------------------------------------------------------- decode split, replayed on the host
+DECODE_CTAS_PER_SM = 2   # decode CTAs one SM holds (110 KB of shared memory each)
+
+
+def decode_tile_split(N: int, K: int, sms: int, ctas_per_sm: int = DECODE_CTAS_PER_SM):
+    """How the decode launch cuts one projection: its (128-row tile, 128-deep
+    block) units, numbered tile-major, are cut into min(resident CTAs, units)
+    contiguous runs, run c = [c*U//PC, (c+1)*U//PC).  Returns (whole, split):
+    tiles that one run covers entirely (stored straight from registers) and
+    tiles that two or more runs share (fp32 partials merged in run order)."""
+    tiles = -(-N // 128)
+    KB = -(-K // 128)
+    U = tiles * KB
+    PC = min(sms * ctas_per_sm, U)
+
+    def run_of(u):
+        return ((u + 1) * PC - 1) // U
+
+    whole = sum(1 for t in range(tiles) if run_of(t * KB) == run_of(t * KB + KB - 1))
+    return whole, tiles - whole

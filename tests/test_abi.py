@@ -165,3 +165,8 @@ def test_embed_rows_refusals_before_any_launch(L):
     assert api.STATUS_NAMES[rc] == "AFFQMM_E_NULL"
     rc = L.affqmm_embed_rows(ctypes.byref(w), 0x200000, 4, 1, 0x4000, 0x300008, None, None)
     assert api.STATUS_NAMES[rc] == "AFFQMM_E_ALIGN"
+
+
+def test_fault_wait_hook_refusal_and_reset(L):
+    assert api.STATUS_NAMES[L.affqmm_test_fault_wait(-5)] == "AFFQMM_E_ARG"
+    assert L.affqmm_test_fault_wait(0) == 0

@@ -127,12 +127,15 @@ def test_run_split_depth(orc, N, K, M):
 
 
 @pytest.mark.parametrize("M", [1, 7, 16])
-def test_one_hot_rows_reproduce_weight_columns(M):
-    """x rows = 2^j e_k give y[m, :] = 2^j W[:, k] exactly (one nonzero product)."""
-    bits, group, N, K = 4, 64, 200, 768
-    _, codes, s, b = synth.problem(bits, group, 1, N, K, seed=77)
+@pytest.mark.parametrize("bits,group", [(4, 64), (2, 128), (3, 64), (5, 32), (6, 64), (8, 32)])
+def test_one_hot_rows_reproduce_weight_columns(orc, bits, group, M):
+    """x rows = 2^j e_k give y[m, :] = 2^j W[:, k] exactly (one nonzero
+    product): the decode kernel's matrix-fragment dequantization, bit for bit,
+    for every width of codes.  W is the oracle's."""
+    N, K = 200, 768
+    _, codes, s, b = synth.problem(bits, group, 1, N, K, seed=77 + bits + group)
     w = api.pack(*cuda(codes, s, b), bits, group)
-    W = api.dequant(w).float()
+    W = synth.from_bits_u16(orc.dequant(bits, group, codes.numpy(), u16(s), u16(b))).float().cuda()
     ks = torch.randint(0, K, (M,), generator=torch.Generator().manual_seed(M))
     js = torch.tensor([0, 3, -2, 1, 0, -1, 2, 0] * 2)[:M]
     x = torch.zeros(M, K)
@@ -151,19 +154,70 @@ def test_deterministic_repeat():
 
 
 @pytest.mark.parametrize("M", [1, 4, 16])
-def test_stacked_equals_separate(M):
+def test_stacked_equals_separate_and_oracle(orc, M):
+    """A stacked call (the q/k/v shapes of a layer at a short depth, one
+    launch) gives each projection the bits of its own call, and each output
+    lies within the tolerance of the oracle's projection."""
     bits, group, K = 4, 64, 1024
     g = synth.generator(55)
-    ws, singles = [], []
-    x = synth.activations(M, K, g).cuda()
+    ws, singles, tables = [], [], []
+    xc = synth.activations(M, K, g)
+    x = xc.cuda()
     for N in (384, 100, 1024):
         codes, s, b = synth.affine_table(bits, group, N, K, g)
         w = api.pack(*cuda(codes, s, b), bits, group)
         ws.append(w)
+        tables.append((codes, s, b))
         singles.append(api.run(w, x))
     ys = api.run_stacked(ws, x)
-    for a, c in zip(ys, singles):
+    for i, (a, c, (codes, s, b)) in enumerate(zip(ys, singles, tables)):
         assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+        assert_within_tolerance(a, oracle_y(orc, bits, group, xc, codes, s, b), f"stacked {i} M={M}")
+
+
+def test_stacked_gate_up_halves_against_oracle(orc):
+    """The gate/up decode configuration as two stacked halves of 15360 rows
+    (one launch over both), each against the oracle."""
+    c = synth.GATE_UP_DECODE
+    bits, group, K = c["bits"], c["group"], c["K"]
+    g = synth.generator(c["seed"] + 500)
+    xc = synth.activations(1, K, g)
+    tables = [synth.affine_table(bits, group, c["N"] // 2, K, g) for _ in range(2)]
+    ws = [api.pack(*cuda(*t), bits, group) for t in tables]
+    ys = api.run_stacked(ws, xc.cuda())
+    for i, (y, (codes, s, b)) in enumerate(zip(ys, tables)):
+        assert_within_tolerance(y, oracle_y(orc, bits, group, xc, codes, s, b, nthreads=16), f"gate/up half {i}")
+
+
+@pytest.mark.parametrize("M", [4, 20])
+def test_non_finite_activations_propagate(orc, M):
+    """Infinite and NaN activations propagate as IEEE arithmetic does: an
+    output is NaN exactly where the oracle's float64 sum is NaN and infinite
+    with the oracle's sign; rows with finite activations stay within the
+    tolerance.  (M = 4 runs the decode kernel, M = 20 the prompt kernel.)"""
+    bits, group, N, K = 4, 64, 300, 640
+    x, codes, s, b = synth.problem(bits, group, M, N, K, seed=4242 + M)
+    xf = x.float()
+    xf[1, 7] = float("inf")                  # a positive infinity
+    xf[2, 130] = float("nan")                # a NaN
+    xf[3, 5], xf[3, 600] = float("-inf"), float("inf")   # both signs: inf - inf where the weights agree in sign
+    x = xf.to(torch.bfloat16)
+    w = api.pack(*cuda(codes, s, b), bits, group)
+    y = api.run(w, x.cuda()).float().cpu().numpy().astype(np.float64)
+    y_ref = oracle_y(orc, bits, group, x, codes, s, b)
+    bad_rows = [1, 2, 3]
+    for m in bad_rows:
+        assert np.array_equal(np.isnan(y[m]), np.isnan(y_ref[m])), f"row {m}: NaN pattern differs"
+        inf = np.isinf(y_ref[m])
+        assert np.array_equal(np.isinf(y[m]), inf), f"row {m}: infinity pattern differs"
+        assert np.array_equal(np.sign(y[m][inf]), np.sign(y_ref[m][inf])), f"row {m}: infinity signs differ"
+        assert not np.any(np.isfinite(y_ref[m])), "every output of a row with a non-finite input is non-finite"
+    assert np.isnan(y_ref[3]).any() and np.isinf(y_ref[3]).any()
+    ok_rows = [m for m in range(M) if m not in bad_rows]
+    got = api.run(w, x.cuda())
+    from helpers import tolerance_report
+    ok, worst, nbad = tolerance_report(u16(got)[ok_rows], y_ref[ok_rows])
+    assert ok, f"finite rows: {nbad} outputs out of tolerance (worst {worst:.3f})"
 
 
 def test_empty_and_degenerate_shapes():

@@ -58,6 +58,18 @@ def test_noalloc_matches_run_on_two_calls_in_a_row():
         assert torch.equal(y.view(torch.int16), r.view(torch.int16)), f"{what}: differs from affqmm_run"
 
 
+def test_noalloc_against_the_oracle(orc):
+    """The same two cases, each output against the CPU oracle's projection."""
+    for bits, group, M, N, K, seed in CASES:
+        x, codes, s, b = synth.problem(bits, group, M, N, K, seed)
+        w = api.pack(codes.cuda(), s.cuda(), b.cuda(), bits, group)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        api.run_noalloc(w, x.cuda(), y)
+        torch.cuda.synchronize()
+        y_ref = orc.qmm(bits, group, u16(x), codes.numpy(), u16(s), u16(b), nthreads=16)
+        assert_within_tolerance(y, y_ref, f"noalloc {bits}b g{group} M={M} N={N} K={K} against the oracle")
+
+
 def test_noalloc_refuses_beyond_its_scratch():
     w, x = _problem(4, 64, 17, 256, 256, 23)
     y = torch.empty(17, 256, dtype=torch.bfloat16, device="cuda")
