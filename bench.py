@@ -17,10 +17,10 @@ over one batch of synthetic input with the weights resident in HBM:
 the decode workloads and TFLOP/s for the prompt chunk.  Weight copies rotate
 so that the bytes touched between two reads of one copy exceed the 129 MB L2.
 Steps are replayed from CUDA graphs and timed with CUDA events on the stream
-that launches them.  `e2e` times the same steps through the Python API with
-the activations uploaded from pinned host memory and the outputs read back
-every step (AFFQMM_E2E_HOST_CALL=1: through affqmm_run_host instead, one C
-call per projection with host buffers).  `--impl reference` times the CPU
+that launches them.  `e2e` times the same steps end to end through the C
+ABI's host-buffer call (affqmm_run_host: x uploaded from pinned host memory,
+the projection, y read back, one call per projection); the exact-codes form
+and the embedding gather use the Python API with torch's copies.  `--impl reference` times the CPU
 oracle on a bounded sample of the same workload on the host cores.  Under torchrun every rank runs an
 independent replica (the path needs no exchange) and rank 0 reports the
 aggregate over ranks with the slowest rank's time.
@@ -228,10 +228,6 @@ class Case:
         else:
             self.api.run(self.ws[i % self.copies], self.x, y=self.y, workspace=workspace)
 
-    def run_host(self, i: int, workspace, x_host, y_host):
-        """One C call: x from host memory into self.x, the projection, self.y back to y_host."""
-        self.api.run_host(self.ws[i % self.copies], x_host, y_host, self.x, self.y, workspace=workspace)
-
     @property
     def packed_bytes(self) -> int:   # codes + bf16 scale and bias per group
         return self.N * self.K * self.bits // 8 + 4 * self.N * self.K // self.group
@@ -275,11 +271,6 @@ class Workload:
     def step(self, i: int):
         for c in self.cases:
             c.run(i, self.workspace)
-
-    def step_host(self, i: int, h_in, h_out):
-        """The step through affqmm_run_host: each case's x from host memory, y back to it."""
-        for c, hx, hy in zip(self.cases, h_in, h_out):
-            c.run_host(i, self.workspace, hx, hy)
 
     @property
     def launches_per_step(self) -> int:
@@ -463,7 +454,6 @@ class EmbedRows(Workload):
 
     launches_per_step = 1
     kernels_per_step = 1
-    step_host = None  # no host-buffer entry point: e2e uploads the ids and reads the rows back with torch copies
 
     @property
     def packed_row_bytes(self) -> int:
@@ -550,10 +540,46 @@ def sustain_for_clocks(graphs, device, seconds: float = 1.0):
         torch.cuda.synchronize(device)
 
 
+class HostCalls:
+    """One step of a workload as C calls of affqmm_run_host with host buffers:
+    per projection, x is uploaded from pinned host memory, the projection runs
+    and y is read back into pinned host memory -- one call of the C ABI, its
+    arguments marshalled once (ctypes, no per-call Python checks)."""
+
+    def __init__(self, wl, h_in, h_out, stream_ptr: int):
+        import ctypes
+        api = wl.api
+        L = api.lib()
+        self.fn = L.affqmm_run_host
+        self.steps = []   # per weight copy: the argument tuples of every case
+        need = max(api.workspace_bytes(c.ws[0], c.M) for c in wl.cases)
+        buf = wl.workspace.get(need)
+        ws_ptr, ws_n = (buf.data_ptr() if need else None), buf.numel()
+        self._keep = []
+        copies = max(c.copies for c in wl.cases)
+        for i in range(copies):
+            calls = []
+            for c, hx, hy in zip(wl.cases, h_in, h_out):
+                cw = c.ws[i % c.copies].cstruct()
+                self._keep.append(cw)
+                calls.append((ctypes.byref(cw), hx.data_ptr(), c.M, hy.data_ptr(), c.x.data_ptr(), c.y.data_ptr(),
+                              ws_ptr, ws_n, stream_ptr))
+            self.steps.append(calls)
+
+    def step(self, i: int):
+        fn = self.fn
+        for args in self.steps[i % len(self.steps)]:
+            rc = fn(*args)
+            if rc:
+                raise RuntimeError(f"affqmm_run_host failed with status {rc}")
+
+
 def time_e2e(wl, steps: int, device):
-    """Same steps through the public API with host buffers: activations uploaded
-    from pinned host memory and outputs read back to pinned host memory every
-    step, inside the timed region."""
+    """Same steps end to end with host buffers: activations uploaded from
+    pinned host memory and outputs read back to pinned host memory every step,
+    inside the timed region.  Projections go through the C ABI's host-buffer
+    call (affqmm_run_host); the exact-codes form and the embedding gather,
+    which have none, go through the Python API with torch's copies around it."""
     import torch
     ins, outs = wl.e2e_io()
     h_in = [t.detach().cpu().pin_memory() for t in ins]
@@ -561,19 +587,23 @@ def time_e2e(wl, steps: int, device):
     bi = sum(t.numel() * t.element_size() for t in h_in)
     bo = sum(t.numel() * t.element_size() for t in h_out)
     stream = torch.cuda.current_stream(device)
-    # The C call with host buffers (affqmm_run_host, `wl.step_host`) measured slower on GB300 than torch's
-    # copies around affqmm_run (1760 against 2586 GB/s on the 241-launch decode step), so the copies stay.
-    host_call = getattr(wl, "step_host", None) if os.environ.get("AFFQMM_E2E_HOST_CALL") == "1" else None
+    cases = getattr(wl, "cases", [])
+    host = None
+    if cases and not any(getattr(c, "exact", False) for c in cases):
+        host = HostCalls(wl, h_in, h_out, int(stream.cuda_stream))
     for i in range(3):
-        wl.step(i)
+        if host is not None:
+            host.step(i)
+        else:
+            wl.step(i)
     torch.cuda.synchronize(device)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record(stream)
     for i in range(steps):
-        if host_call is not None:
-            host_call(i, h_in, h_out)
+        if host is not None:
+            host.step(i)
             continue
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
@@ -583,7 +613,8 @@ def time_e2e(wl, steps: int, device):
     e1.record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t0
-    return max(wall, e0.elapsed_time(e1) * 1e-3), bi, bo
+    via = "affqmm_run_host (C ABI, host buffers)" if host is not None else "Python API + torch copies"
+    return max(wall, e0.elapsed_time(e1) * 1e-3), bi, bo, via
 
 
 # ----------------------------------------------------------------------------- oracle
@@ -645,8 +676,9 @@ class OracleSample:
         if self.exact:
             return (f"{reps} x {rows} of {self.N} output rows of one projection of the workload (M={self.M}, "
                     f"K={self.K}, {self.bits}-bit g{self.group}); float64 exact-codes oracle on one thread")
+        how = f"threaded over rows on {self.threads} cores" if self.threads > 1 else "on one thread"
         return (f"{reps} x {rows} of {self.N} output rows of one projection of the workload (M={self.M}, "
-                f"K={self.K}, {self.bits}-bit g{self.group}); float64 oracle threaded over rows")
+                f"K={self.K}, {self.bits}-bit g{self.group}); float64 oracle {how}")
 
     def rate(self, seconds: float):
         rows = self.rows_for(seconds)
@@ -766,10 +798,10 @@ def main(argv=None):
     e2e = None
     if not args.no_e2e:
         e2e_steps = min(steps, 2000)
-        t_e2e, bi, bo = time_e2e(wl, e2e_steps, device)
+        t_e2e, bi, bo, via = time_e2e(wl, e2e_steps, device)
         t_e2e = reduce_max(dist, t_e2e, device)
         e2e = {"value": aggregate(wl.units_per_step * e2e_steps, world, t_e2e) / wl.scale, "unit": wl.unit,
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps, "via": via}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -777,6 +809,11 @@ def main(argv=None):
         r, sample, dt = smp.rate(args.cpu_seconds)
         cpu = {"value": r, "unit": wl.unit, "cores": smp.threads, "kind": "oracle", "sample": sample,
                "seconds": round(dt, 2)}
+        if smp.threads > 1:   # the same oracle on one host core
+            smp.threads = 1
+            r1, sample1, dt1 = smp.rate(args.cpu_seconds)
+            cpu["single_thread"] = {"value": r1, "unit": wl.unit, "cores": 1, "sample": sample1,
+                                    "seconds": round(dt1, 2)}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world, "steps": steps,

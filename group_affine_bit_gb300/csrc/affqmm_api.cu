@@ -273,8 +273,17 @@ int check_stack(int count, const affqmm_weight* ws) {
     return AFFQMM_OK;
 }
 
+int check_workspace(size_t need, void* workspace, size_t ws_bytes) {
+    if (need == 0) return AFFQMM_OK;
+    if (!workspace || ws_bytes < need) return AFFQMM_E_WORKSPACE;
+    if (!aligned(workspace, 256)) return AFFQMM_E_ALIGN;
+    return AFFQMM_OK;
+}
+
+// Validate everything, plan, and (unless `dry`) enqueue the launches.  A dry
+// run returns the status the real call would return before any launch.
 int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, uint16_t* const* ys,
-             void* workspace, size_t ws_bytes, void* stream, bool exact = false) {
+             void* workspace, size_t ws_bytes, void* stream, bool exact = false, bool dry = false) {
     int rc = check_stack(count, ws);
     if (rc) return rc;
     if (M < 0 || M > AFFQMM_MAX_M || (exact && M > kDecodeRows)) return AFFQMM_E_M;
@@ -296,22 +305,18 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (K == 0) {  // an empty sum: every output is +0
+        if (dry) return AFFQMM_OK;
         for (int i = 0; i < count; ++i)
             if (ws[i].N > 0 && cudaMemsetAsync(ys[i], 0, (size_t)M * ws[i].N * 2, st) != cudaSuccess)
                 return AFFQMM_E_CUDA;
         return AFFQMM_OK;
     }
-    size_t need = 0;
-    rc = workspace_for(count, ws, M, &need);
-    if (rc) return rc;
-    if (need > 0) {
-        if (!workspace || ws_bytes < need) return AFFQMM_E_WORKSPACE;
-        if (!aligned(workspace, 256)) return AFFQMM_E_ALIGN;
-    }
     if (M <= kDecodeRows) {
         DecodePlan plan;
         rc = plan_decode(*d, count, ws, M, &plan);
         if (rc) return rc;
+        rc = check_workspace(plan.ws_bytes, workspace, ws_bytes);
+        if (rc || dry) return rc;
         bind_workspace(&plan, workspace);
         for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i];
         plan.p.x = x;
@@ -322,7 +327,15 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
             return AFFQMM_E_CUDA;
         return AFFQMM_OK;
     }
-    // Prompt rows: chunks of up to 128 rows on the tensor-core kernel.
+    // Prompt rows: chunks of up to 128 rows on the tensor-core kernel.  The
+    // first chunk is the largest: its plan sizes the workspace.
+    {
+        PromptPlan first;
+        rc = plan_prompt(*d, count, ws, std::min<int64_t>(M, kPromptRows), &first);
+        if (rc) return rc;
+        rc = check_workspace(first.ws_bytes, workspace, ws_bytes);
+        if (rc || dry) return rc;
+    }
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     for (int64_t m0 = 0; m0 < M; m0 += kPromptRows) {
         const int64_t mc = std::min(kPromptRows, M - m0);
@@ -431,28 +444,17 @@ int affqmm_run_host(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16
     if (M < 0 || M > AFFQMM_MAX_M) return AFFQMM_E_M;
     if (M == 0 || w->N == 0) return AFFQMM_OK;
     if (!y || !y_dev) return AFFQMM_E_NULL;
-    if (!aligned(y_dev, 2)) return AFFQMM_E_ALIGN;
-    if (w->K > 0) {
-        if (!x || !x_dev) return AFFQMM_E_NULL;
-        if (!aligned(x_dev, 16)) return AFFQMM_E_ALIGN;
-    }
-    DeviceInfo* d = nullptr;
-    rc = device_info(&d);
+    if (w->K > 0 && !x) return AFFQMM_E_NULL;
+    uint16_t* ys[1] = {y_dev};
+    // every check of the device call (x_dev, y_dev, workspace, device) before anything is enqueued
+    rc = run_impl(1, w, x_dev, M, ys, workspace, ws_bytes, stream, false, true);
     if (rc) return rc;
-    size_t need = 0;
-    rc = workspace_for(1, w, M, &need);
-    if (rc) return rc;
-    if (need > 0) {
-        if (!workspace || ws_bytes < need) return AFFQMM_E_WORKSPACE;
-        if (!aligned(workspace, 256)) return AFFQMM_E_ALIGN;
-    }
     CopyHtoDFn htod = copy_htod();
     CopyDtoHFn dtoh = copy_dtoh();
     if (!htod || !dtoh) return AFFQMM_E_CUDA;
     CUstream cs = static_cast<CUstream>(stream);
     if (w->K > 0 && htod(reinterpret_cast<CUdeviceptr>(x_dev), x, (size_t)M * (size_t)w->K * 2, cs) != CUDA_SUCCESS)
         return AFFQMM_E_CUDA;
-    uint16_t* ys[1] = {y_dev};
     rc = run_impl(1, w, x_dev, M, ys, workspace, ws_bytes, stream);
     if (rc) return rc;
     if (dtoh(y, reinterpret_cast<CUdeviceptr>(y_dev), (size_t)M * (size_t)w->N * 2, cs) != CUDA_SUCCESS)
