@@ -65,6 +65,11 @@ class Oracle:
         lib.oracle_qmm_groupsum.restype = ctypes.c_int
         lib.oracle_qmm_groupsum.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64,
                                             _u16p, _u8p, _u16p, _u16p, _f64p, _f64p]
+        lib.oracle_qmm_groupsum_given.restype = ctypes.c_int
+        lib.oracle_qmm_groupsum_given.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _u16p,
+                                                  ctypes.POINTER(ctypes.c_float), _u8p, _u16p, _u16p, _f64p]
+        lib.oracle_geglu.restype = None
+        lib.oracle_geglu.argtypes = [_i64, _u16p, _u16p, ctypes.c_int, _u16p, _u16p]
         lib.oracle_embed_rows.restype = ctypes.c_int
         lib.oracle_embed_rows.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _u8p, _u16p, _u16p,
                                           ctypes.POINTER(ctypes.c_int32), _i64, ctypes.c_int, ctypes.c_uint16, _u16p]
@@ -150,6 +155,56 @@ class Oracle:
             with ThreadPoolExecutor(nthreads) as ex:
                 list(ex.map(lambda t: rows(cuts[t], cuts[t + 1]), range(nthreads)))
         return y, mag
+
+    def qmm_groupsum_given(self, bits, group, x, xsums, codes, scales, biases, nthreads: int = 1):
+        """The exact-codes form with the group sums of x given: xsums float32
+        [M, K/g].  nthreads > 1 splits the output rows n into slices, one C call
+        per slice from a thread pool."""
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        xsums = np.ascontiguousarray(xsums, dtype=np.float32)
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        biases = np.ascontiguousarray(biases, dtype=np.uint16)
+        M, K = x.shape
+        N = codes.shape[0]
+        if xsums.shape != (M, K // group):
+            raise ValueError("xsums must be [M, K/group]")
+        y = np.empty((M, N), dtype=np.float64)
+
+        def rows(n0, n1):
+            yy = np.empty((M, n1 - n0), dtype=np.float64)
+            rc = self.lib.oracle_qmm_groupsum_given(bits, group, M, n1 - n0, K, _ptr(x, _u16p),
+                                                    xsums.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                                    _ptr(codes[n0:n1], _u8p), _ptr(scales[n0:n1], _u16p),
+                                                    _ptr(biases[n0:n1], _u16p), _ptr(yy, _f64p))
+            if rc:
+                raise ValueError(f"oracle_qmm_groupsum_given rejected its arguments (rc={rc})")
+            y[:, n0:n1] = yy
+
+        nthreads = max(1, min(int(nthreads), N))
+        if nthreads == 1:
+            rows(0, N)
+        else:
+            from concurrent.futures import ThreadPoolExecutor
+            cuts = [N * t // nthreads for t in range(nthreads + 1)]
+            with ThreadPoolExecutor(nthreads) as ex:
+                list(ex.map(lambda t: rows(cuts[t], cuts[t + 1]), range(nthreads)))
+        return y
+
+    # -- GeGLU ---------------------------------------------------------------------
+    def geglu(self, gate, up, tanh_ulps: int = 4):
+        """h = gelu_approx(gate) * up as bf16 operations (bit patterns in, bit
+        patterns out): returns (h_lo, h_hi), the results for the bf16 roundings
+        of tanh on either side of an fp32 tanh within tanh_ulps ulps."""
+        gate = np.ascontiguousarray(gate, dtype=np.uint16)
+        up = np.ascontiguousarray(up, dtype=np.uint16)
+        if gate.shape != up.shape:
+            raise ValueError("gate and up differ in shape")
+        lo = np.empty(gate.shape, dtype=np.uint16)
+        hi = np.empty(gate.shape, dtype=np.uint16)
+        self.lib.oracle_geglu(gate.size, _ptr(gate, _u16p), _ptr(up, _u16p), int(tanh_ulps), _ptr(lo, _u16p),
+                              _ptr(hi, _u16p))
+        return lo, hi
 
     # -- scaled embedding rows -------------------------------------------------
     def embed_rows(self, bits, group, codes, scales, biases, ids, scale=None) -> np.ndarray:

@@ -16,6 +16,8 @@
  *   4. scaled embedding rows bf16(W[n,k] * scale) -- "cuda gemma4: images on
  *      the 12B" page, the embed_rows commit (the weight rounded first, then
  *      its product with the bf16 scale rounded again).
+ *   5. the exact-codes form with producer-written group sums, and mlx_lm's
+ *      GeGLU as bf16 operations (the fused gate/up epilogue) -- see oracle.h.
  *
  * The arithmetic is deliberately plain: no blocking, no vectorization, no
  * reordering of the sum.  Threads only split independent output rows.
@@ -263,4 +265,73 @@ int oracle_embed_rows(int bits, int group, int64_t N, int64_t K,
         }
     }
     return 0;
+}
+
+int oracle_qmm_groupsum_given(int bits, int group, int64_t M, int64_t N, int64_t K,
+                              const uint16_t* x, const float* xsums, const uint8_t* codes,
+                              const uint16_t* scales, const uint16_t* biases, double* y) {
+    int rc = check_args(bits, group, N, K);
+    if (rc) return rc;
+    if (M < 0) return -3;
+    const int64_t G = K / group;
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t* xr = x + m * K;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < G; ++j) {
+                double s = oracle_bf16_to_double(scales[n * G + j]);
+                double b = oracle_bf16_to_double(biases[n * G + j]);
+                double sqx = 0.0;
+                for (int64_t k = j * group; k < (j + 1) * group; ++k)
+                    sqx += (double)codes[n * K + k] * oracle_bf16_to_double(xr[k]);
+                acc += s * sqx + b * (double)xsums[m * G + j];
+            }
+            y[m * N + n] = acc;
+        }
+    }
+    return 0;
+}
+
+/* bf16 of an exact real given as a double: the products of two bf16 values,
+ * the cube of one and the sum of two are exact in double (at most 24
+ * significant bits, or an exponent gap beyond which the smaller addend cannot
+ * move the bf16 rounding of the larger), so one rounding here is the single
+ * rounding of the exact result. */
+static uint16_t bf_round(double v) { return oracle_bf16_from_double(v); }
+static double bf(uint16_t h) { return oracle_bf16_to_double(h); }
+
+/* The steps after tanh (t the bf16 tanh's value): e = bf16(1 + t),
+ * p = bf16(0.5 g), r = bf16(p e), h = bf16(r up). */
+static uint16_t geglu_tail(uint16_t g, double t, uint16_t up) {
+    uint16_t e = bf_round(1.0 + t);
+    uint16_t p = bf_round(0.5 * bf(g));
+    uint16_t r = bf_round(bf(p) * bf(e));
+    return bf_round(bf(r) * bf(up));
+}
+
+void oracle_geglu(int64_t n, const uint16_t* gate, const uint16_t* up, int tanh_ulps,
+                  uint16_t* h_lo, uint16_t* h_hi) {
+    const uint16_t c1 = bf_round(0.044715);
+    const uint16_t c2 = bf_round(sqrt(2.0 / 3.14159265358979323846));
+    for (int64_t i = 0; i < n; ++i) {
+        const uint16_t g = gate[i];
+        const double gv = bf(g);
+        uint16_t c3 = bf_round(gv * gv * gv);
+        uint16_t a = bf_round(bf(c1) * bf(c3));
+        uint16_t z = bf_round(gv + bf(a));
+        uint16_t u = bf_round(bf(c2) * bf(z));
+        const double tv = tanh(bf(u));
+        /* the fp32 tanh of a GPU is tv within tanh_ulps fp32 ulps; its bf16
+         * rounding is one of the roundings of the interval's ends */
+        double d = 0.0;
+        if (isfinite(tv) && tv != 0.0) {
+            int e = 0;
+            (void)frexp(tv, &e);
+            d = ldexp((double)tanh_ulps, e - 24);
+        }
+        uint16_t t_lo = bf_round(tv - d), t_hi = bf_round(tv + d);
+        if (isnan(tv)) t_lo = t_hi = bf_round(tv);
+        h_lo[i] = geglu_tail(g, bf(t_lo), up[i]);
+        h_hi[i] = geglu_tail(g, bf(t_hi), up[i]);
+    }
 }

@@ -71,6 +71,34 @@ int oracle_qmm_groupsum(int bits, int group, int64_t M, int64_t N, int64_t K,
                         const uint16_t* scales, const uint16_t* biases,
                         double* y_gs, double* mag);
 
+/* The exact-codes form with the group sums of x supplied by the caller, as
+ * the kernel that produced x writes them ("Gemma 4 12B on the native Metal
+ * engine" page, the commit where the norm, merge, attention-tail, geglu and
+ * dense-tail kernels write the next projection's group sums):
+ * y[m,n] = sum_j ( s_j * sum_{k in j} q[n,k]*x[m,k] + b_j * xsums[m,j] ),
+ * in double; xsums is fp32 [M, K/g] and is used as given. */
+int oracle_qmm_groupsum_given(int bits, int group, int64_t M, int64_t N, int64_t K,
+                              const uint16_t* x, const float* xsums, const uint8_t* codes,
+                              const uint16_t* scales, const uint16_t* biases, double* y);
+
+/* mlx_lm's GeGLU on bf16 rows, h = gelu_approx(gate) * up, as MLX evaluates it
+ * on bf16 arrays: every operation's exact result rounded once to bf16, the
+ * constants taken as bf16:
+ *   c3 = bf16(g^3)        c1 = bf16(0.044715)     a = bf16(c1 * c3)
+ *   z  = bf16(g + a)      c2 = bf16(sqrt(2/pi))   u = bf16(c2 * z)
+ *   t  = bf16(tanh(u))    e  = bf16(1 + t)        p = bf16(0.5 * g)
+ *   r  = bf16(p * e)      h  = bf16(r * up)
+ * ("cuda gemma4" page: tf_geglu_rows computes mlx_lm's gelu_approx(gate) * up
+ * as MLX's bf16 ops; "Gemma 4 12B on the native Metal engine" page: geglu as
+ * the gate/up projection's epilogue, the same bits as apart).  tanh is the
+ * double library function.  A GPU's fp32 tanh is within `tanh_ulps` fp32
+ * ulps of the exact value, so where the exact tanh lies that close to a bf16
+ * rounding boundary the bf16 t has two possible values: h_lo takes the one
+ * below, h_hi the one above (equal everywhere else).  NaN and infinities
+ * propagate as IEEE arithmetic does. */
+void oracle_geglu(int64_t n, const uint16_t* gate, const uint16_t* up, int tanh_ulps,
+                  uint16_t* h_lo, uint16_t* h_hi);
+
 /* Scaled embedding rows: out[t,k] = bf16( bf16(s*q + b) * scale ) for the
  * table row n = ids[t] -- two roundings, each of an exact value: the weight
  * (as oracle_dequant_one) and then its exact product with the bf16 scale.

@@ -396,6 +396,134 @@ def pin_embed_rows_special_cases(orc, seed=23):
                 assert bf16_value(int(out[t, k])) == 8 * bf16_value(int(W[n, k]))
 
 
+def pin_qmm_groupsum_given_bruteforce(orc, seed=29):
+    """The exact-codes form with supplied group sums of x, against exact
+    rational arithmetic: sum_g (s_g * sum q x + b_g * xs_g), the codes exact and
+    the sums taken as given (here: fp32 values that are not the exact sums, so
+    that a form that recomputes them from x fails)."""
+    rng = np.random.default_rng(seed)
+    for bits, group, M, N, K in [(4, 64, 2, 3, 128), (3, 32, 1, 2, 96), (8, 128, 2, 2, 256), (5, 32, 1, 3, 64)]:
+        x, codes, s, b = _small_problem(rng, bits, group, M, N, K)
+        G = K // group
+        xs = rng.normal(0, 8, (M, G)).astype(np.float32)
+        y = orc.qmm_groupsum_given(bits, group, x, xs, codes, s, b)
+        for m in range(M):
+            for n in range(N):
+                exact = Fraction(0)
+                amag = Fraction(0)
+                for j in range(G):
+                    sv, bv = bf16_value(int(s[n, j])), bf16_value(int(b[n, j]))
+                    xv = [bf16_value(int(v)) for v in x[m, j * group:(j + 1) * group]]
+                    qs = [int(q) for q in codes[n, j * group:(j + 1) * group]]
+                    term_q = sv * sum((q * v for q, v in zip(qs, xv)), Fraction(0))
+                    term_b = bv * Fraction(float(xs[m, j]))
+                    exact += term_q + term_b
+                    amag += abs(term_q) + abs(term_b)
+                assert abs(Fraction(float(y[m, n])) - exact) <= amag * Fraction(1, 2 ** 44), (bits, group, m, n)
+    # with the exact sums of x supplied, the form equals the exact-codes form within double rounding
+    x, codes, s, b = _small_problem(rng, 4, 64, 2, 8, 256)
+    xv = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    xs = xv.reshape(2, 4, 64).sum(axis=2).astype(np.float32)   # the sums of x rounded to fp32
+    y = orc.qmm_groupsum_given(4, 64, x, xs, codes, s, b)
+    y_gs, mag = orc.qmm_groupsum(4, 64, x, codes, s, b)
+    bound = np.abs(xs.astype(np.float64) - xv.reshape(2, 4, 64).sum(axis=2))
+    bsum = np.abs(torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).double().numpy())
+    assert np.all(np.abs(y - y_gs) <= (bound @ bsum.T) + 1e-12 * mag + 1e-300)
+
+
+# -- GeGLU (mlx_lm's gelu_approx(gate) * up as bf16 operations) ------------------
+def _bf16_tensor(bits_u16: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits_u16, dtype=np.uint16).view(np.int16).copy()).view(torch.bfloat16)
+
+
+def _geglu_inputs(rng, n):
+    """bf16 gate/up patterns over many magnitudes, both signs, with zeros,
+    subnormals and the values where tanh saturates."""
+    mags = np.concatenate([rng.normal(0, 1, n // 2), rng.normal(0, 4, n // 4),
+                           np.exp2(rng.uniform(-140, 20, n - n // 2 - n // 4)) * rng.choice([-1, 1], n - n // 2 - n // 4)])
+    gate = bits_from_torch_bf16(torch.from_numpy(mags.astype(np.float32)).to(torch.bfloat16))
+    up = bits_from_torch_bf16(torch.from_numpy(rng.normal(0, 2, n).astype(np.float32)).to(torch.bfloat16))
+    gate[:4] = [0x0000, 0x8000, 0x0001, 0x8001]
+    return gate, up
+
+
+def pin_geglu_against_torch_bf16_ops(orc, seed=31):
+    """Each step of the chain against torch's own bf16 arithmetic (a library:
+    every op on bf16 tensors rounds its fp32 result to bf16; fp32 holds the
+    exact product of two bf16 values and the exact cube of one): torch's
+    result must be one of the oracle's two (they differ only where tanh's
+    rounding is ambiguous)."""
+    rng = np.random.default_rng(seed)
+    gate, up = _geglu_inputs(rng, 200000)
+    lo, hi = orc.geglu(gate, up)
+    g, u = _bf16_tensor(gate), _bf16_tensor(up)
+    gf = g.float()
+    c3 = (gf * gf * gf).to(torch.bfloat16)
+    c1 = torch.tensor(0.044715, dtype=torch.bfloat16)
+    c2 = torch.tensor(math.sqrt(2 / math.pi), dtype=torch.bfloat16)
+    z = g + c1 * c3
+    t = torch.tanh(c2 * z)
+    h = (torch.tensor(0.5, dtype=torch.bfloat16) * g) * (1 + t) * u
+    hb = bits_from_torch_bf16(h)
+    ok = (hb == lo) | (hb == hi)
+    nan = np.isnan(h.float().numpy())
+    ok |= nan & np.isnan(_bf16_tensor(lo).float().numpy())
+    assert np.all(ok), f"{int(np.sum(~ok))} outputs differ from torch's bf16 operations, e.g. gate {gate[~ok][0]:#06x}"
+    amb = np.mean(lo != hi)
+    assert amb < 0.01, f"tanh's rounding is ambiguous on {amb:.3%} of outputs"
+
+
+def pin_geglu_closed_forms(orc, seed=37):
+    """Special cases with closed forms: gate = +-0 gives a zero; gate >= 16
+    saturates tanh to 1 in bf16, so h = bf16(gate * up) exactly; gate <= -16
+    gives 1 + tanh = 0 and h = +-0; |gate| <= 2^-12 leaves 1 + tanh = 1, so
+    h = bf16(bf16(gate / 2) * up)."""
+    rng = np.random.default_rng(seed)
+    n = 4000
+    up = bits_from_torch_bf16(torch.from_numpy(rng.normal(0, 3, n).astype(np.float32)).to(torch.bfloat16))
+    big = np.array([random_bf16(random.Random(i), 4, 40, sign=0) for i in range(n)], dtype=np.uint16)
+    lo, hi = orc.geglu(big, up)
+    for i in range(n):
+        want = rne_bf16_bits(bf16_value(int(big[i])) * bf16_value(int(up[i])),
+                             negative_zero=bool(up[i] & 0x8000))
+        assert lo[i] == want and hi[i] == want, (hex(big[i]), hex(up[i]), hex(lo[i]), hex(want))
+    neg = big | 0x8000
+    lo, hi = orc.geglu(neg, up)
+    assert np.all((lo & 0x7FFF) == 0) and np.all((hi & 0x7FFF) == 0)
+    tiny = np.array([random_bf16(random.Random(7 * i), -120, -12) for i in range(n)], dtype=np.uint16)
+    lo, hi = orc.geglu(tiny, up)
+    for i in range(n):
+        half = rne_bf16_bits(bf16_value(int(tiny[i])) / 2, negative_zero=bool(tiny[i] & 0x8000))
+        want = rne_bf16_bits(bf16_value(half) * bf16_value(int(up[i])),
+                             negative_zero=bool((half ^ up[i]) & 0x8000))
+        assert lo[i] == want and hi[i] == want, (hex(tiny[i]), hex(up[i]), hex(lo[i]), hex(want))
+    zeros = np.array([0x0000, 0x8000] * 4, dtype=np.uint16)
+    lo, _ = orc.geglu(zeros, up[:8])
+    assert np.all((lo & 0x7FFF) == 0)
+
+
+def pin_geglu_near_textbook_gelu(orc, seed=41):
+    """Against the GELU tanh approximation evaluated in float64 (the textbook
+    formula, no roundings): on |gate| <= 6 the bf16 chain stays within
+    2^-6 * (1 + |gate|) of gelu(gate) (up = 1), which a wrong constant, a
+    missing term or swapped operands does not."""
+    rng = np.random.default_rng(seed)
+    gv = rng.uniform(-6, 6, 50000).astype(np.float32)
+    gate = bits_from_torch_bf16(torch.from_numpy(gv).to(torch.bfloat16))
+    one = np.full(gate.shape, 0x3F80, dtype=np.uint16)
+    lo, hi = orc.geglu(gate, one)
+    x = _bf16_tensor(gate).double().numpy()
+    ref = 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))
+    for h in (lo, hi):
+        got = _bf16_tensor(h).double().numpy()
+        assert np.all(np.abs(got - ref) <= 2.0 ** -6 * (1 + np.abs(x))), float(np.max(np.abs(got - ref)))
+    # and gate/up enter in their roles: h(g, u) != h(u, g) in general
+    up = bits_from_torch_bf16(torch.from_numpy(rng.uniform(-6, 6, 50000).astype(np.float32)).to(torch.bfloat16))
+    a, _ = orc.geglu(gate, up)
+    b, _ = orc.geglu(up, gate)
+    assert np.mean(a != b) > 0.5
+
+
 ALL_PINS = [
     pin_bf16_golden,
     pin_bf16_against_torch,
@@ -409,4 +537,8 @@ ALL_PINS = [
     pin_qmm_groupsum_bruteforce,
     pin_embed_rows_exact,
     pin_embed_rows_special_cases,
+    pin_qmm_groupsum_given_bruteforce,
+    pin_geglu_against_torch_bf16_ops,
+    pin_geglu_closed_forms,
+    pin_geglu_near_textbook_gelu,
 ]

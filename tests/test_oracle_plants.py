@@ -69,6 +69,33 @@ PLANTS = {
     # exact-codes form: the codes' products use the next row's codes
     "groupsum_wrong_code_row": ("double q = (double)codes[n * K + k];",
                                 "double q = (double)codes[((n + 1) % N) * K + k];"),
+    # supplied group sums: every activation row takes row 0's sums
+    "given_sums_row0": ("acc += s * sqx + b * (double)xsums[m * G + j];", "acc += s * sqx + b * (double)xsums[j];"),
+    # supplied group sums ignored: recomputed from x (the form the producer's sums replace)
+    "given_sums_recomputed": (
+        "                for (int64_t k = j * group; k < (j + 1) * group; ++k)\n"
+        "                    sqx += (double)codes[n * K + k] * oracle_bf16_to_double(xr[k]);\n"
+        "                acc += s * sqx + b * (double)xsums[m * G + j];",
+        "                double sx = 0.0;\n"
+        "                for (int64_t k = j * group; k < (j + 1) * group; ++k) {\n"
+        "                    sqx += (double)codes[n * K + k] * oracle_bf16_to_double(xr[k]);\n"
+        "                    sx += oracle_bf16_to_double(xr[k]); }\n"
+        "                acc += s * sqx + b * sx;"),
+    # GeGLU: each plant drops one rounding point of the bf16 chain, or changes a constant or an operand
+    "geglu_cube_unrounded": ("uint16_t a = bf_round(bf(c1) * bf(c3));", "uint16_t a = bf_round(bf(c1) * (gv * gv * gv));"),
+    "geglu_product_unrounded": ("uint16_t z = bf_round(gv + bf(a));", "uint16_t z = bf_round(gv + bf(c1) * bf(c3));"),
+    "geglu_sum_unrounded": ("uint16_t u = bf_round(bf(c2) * bf(z));", "uint16_t u = bf_round(bf(c2) * (gv + bf(a)));"),
+    "geglu_scaled_unrounded": ("const double tv = tanh(bf(u));", "const double tv = tanh(bf(c2) * bf(z));"),
+    "geglu_tanh_unrounded": (
+        "        h_lo[i] = geglu_tail(g, bf(t_lo), up[i]);\n        h_hi[i] = geglu_tail(g, bf(t_hi), up[i]);",
+        "        h_lo[i] = geglu_tail(g, tv, up[i]);\n        h_hi[i] = geglu_tail(g, tv, up[i]);"),
+    "geglu_one_plus_unrounded": ("    uint16_t r = bf_round(bf(p) * bf(e));", "    uint16_t r = bf_round(bf(p) * (1.0 + t));"),
+    "geglu_gelu_unrounded": ("    return bf_round(bf(r) * bf(up));", "    return bf_round(bf(p) * bf(e) * bf(up));"),
+    "geglu_constants_unrounded": (
+        "    const uint16_t c1 = bf_round(0.044715);\n    const uint16_t c2 = bf_round(sqrt(2.0 / 3.14159265358979323846));",
+        "    const uint16_t c1 = bf_round(0.044715) + 1;\n    const uint16_t c2 = bf_round(sqrt(2.0 / 3.14159265358979323846)) - 1;"),
+    "geglu_half_dropped": ("    uint16_t p = bf_round(0.5 * bf(g));", "    uint16_t p = g;"),
+    "geglu_up_ignored": ("    return bf_round(bf(r) * bf(up));", "    return r;"),
     # the scale and bias patterns swapped
     "swapped_scale_bias": ("double sd = oracle_bf16_to_double(s);\n    double bd = oracle_bf16_to_double(b);",
                            "double sd = oracle_bf16_to_double(b);\n    double bd = oracle_bf16_to_double(s);"),
