@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
             "affqmm_run_exact": (i32, [wp, vp, i64, vp, vp, ctypes.c_size_t, vp]),
             "affqmm_embed_rows": (i32, [wp, vp, i64, i32, ctypes.c_uint16, vp, vp, vp]),
             "affqmm_test_fault_wait": (i32, [i64]),
+            "affqmm_run_exact_sums": (i32, [wp, vp, vp, i64, vp, vp, ctypes.c_size_t, vp]),
+            "affqmm_run_geglu": (i32, [wp, vp, vp, i64, i32, vp, vp, ctypes.c_size_t, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -235,6 +237,58 @@ def run_exact(w: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, w
     _check(lib().affqmm_run_exact(ctypes.byref(cw), x.data_ptr(), M, y.data_ptr(), buf.data_ptr() if need else None,
                                   buf.numel(), sp), "affqmm_run_exact")
     return y
+
+
+FORM_ROUNDED, FORM_EXACT, FORM_EXACT_SUMS = 0, 1, 2
+
+
+def _check_xsums(xsums: torch.Tensor, M: int, w: PackedWeight, x: torch.Tensor):
+    G = w.K // w.group
+    if (not xsums.is_cuda or xsums.dtype != torch.float32 or tuple(xsums.shape) != (M, G)
+            or not xsums.is_contiguous() or xsums.device != x.device):
+        raise ValueError(f"xsums must be a contiguous CUDA float32 [{M}, {G}] tensor on {x.device}")
+
+
+def run_exact_sums(w: PackedWeight, x: torch.Tensor, xsums: torch.Tensor, y: torch.Tensor | None = None,
+                   workspace: Workspace | None = None, stream=None) -> torch.Tensor:
+    """affqmm_run_exact_sums (M <= 16): the exact-codes form with the group sums
+    of x (float32 [M, K/group]) as the kernel that produced x wrote them."""
+    _check_x(x, w.K)
+    M = x.shape[0]
+    _check_xsums(xsums, M, w, x)
+    dev = x.get_device()
+    if y is None:
+        y = torch.empty(M, w.N, dtype=torch.bfloat16, device=x.device)
+    sp = _stream_ptr(stream, dev)
+    ws = workspace or default_workspace(dev, sp)
+    need = workspace_bytes(w, M)
+    buf = ws.get(need)
+    cw = w.cstruct()
+    _check(lib().affqmm_run_exact_sums(ctypes.byref(cw), x.data_ptr(), xsums.data_ptr(), M, y.data_ptr(),
+                                       buf.data_ptr() if need else None, buf.numel(), sp), "affqmm_run_exact_sums")
+    return y
+
+
+def run_geglu(w: PackedWeight, x: torch.Tensor, form: int = FORM_ROUNDED, xsums: torch.Tensor | None = None,
+              h: torch.Tensor | None = None, workspace: Workspace | None = None, stream=None) -> torch.Tensor:
+    """affqmm_run_geglu (M <= 16): a gate/up stack (rows interleaved in 16-row
+    blocks) with GeGLU as its epilogue; returns h bf16 [M, N/2]."""
+    _check_x(x, w.K)
+    M = x.shape[0]
+    if form == FORM_EXACT_SUMS:
+        _check_xsums(xsums, M, w, x)
+    dev = x.get_device()
+    if h is None:
+        h = torch.empty(M, w.N // 2, dtype=torch.bfloat16, device=x.device)
+    sp = _stream_ptr(stream, dev)
+    ws = workspace or default_workspace(dev, sp)
+    need = workspace_bytes(w, M)
+    buf = ws.get(need)
+    cw = w.cstruct()
+    xs = xsums.data_ptr() if (form == FORM_EXACT_SUMS and xsums is not None) else None
+    _check(lib().affqmm_run_geglu(ctypes.byref(cw), x.data_ptr(), xs, M, int(form), h.data_ptr(),
+                                  buf.data_ptr() if need else None, buf.numel(), sp), "affqmm_run_geglu")
+    return h
 
 
 def run_host(w: PackedWeight, x: torch.Tensor, y: torch.Tensor, x_dev: torch.Tensor, y_dev: torch.Tensor,

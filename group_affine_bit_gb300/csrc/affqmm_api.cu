@@ -282,11 +282,24 @@ int check_workspace(size_t need, void* workspace, size_t ws_bytes) {
 
 // Validate everything, plan, and (unless `dry`) enqueue the launches.  A dry
 // run returns the status the real call would return before any launch.
+// Options of the decode-only forms: exact codes, the caller's group sums of
+// x, the GeGLU epilogue.
+struct Form {
+    bool exact = false;
+    const float* xsums = nullptr;
+    int epi = 0;
+};
+
 int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, uint16_t* const* ys,
-             void* workspace, size_t ws_bytes, void* stream, bool exact = false, bool dry = false) {
+             void* workspace, size_t ws_bytes, void* stream, Form form = Form(), bool dry = false) {
     int rc = check_stack(count, ws);
     if (rc) return rc;
-    if (M < 0 || M > AFFQMM_MAX_M || (exact && M > kDecodeRows)) return AFFQMM_E_M;
+    const bool decode_only = form.exact || form.epi != 0;
+    if (M < 0 || M > AFFQMM_MAX_M || (decode_only && M > kDecodeRows)) return AFFQMM_E_M;
+    if (form.epi != 0)
+        for (int i = 0; i < count; ++i)
+            if (ws[i].N % 32 != 0) return AFFQMM_E_SHAPE;  // gate/up rows interleaved in 16-row blocks
+    if (form.xsums && !aligned(form.xsums, 4)) return AFFQMM_E_ALIGN;
     if (M == 0) return AFFQMM_OK;
     const int64_t K = ws[0].K;
     int64_t total_n = 0;
@@ -307,7 +320,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
     if (K == 0) {  // an empty sum: every output is +0
         if (dry) return AFFQMM_OK;
         for (int i = 0; i < count; ++i)
-            if (ws[i].N > 0 && cudaMemsetAsync(ys[i], 0, (size_t)M * ws[i].N * 2, st) != cudaSuccess)
+            if (ws[i].N > 0 && cudaMemsetAsync(ys[i], 0, (size_t)M * ws[i].N * 2 / (form.epi ? 2 : 1), st) != cudaSuccess)
                 return AFFQMM_E_CUDA;
         return AFFQMM_OK;
     }
@@ -320,10 +333,12 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         bind_workspace(&plan, workspace);
         for (int i = 0; i < count; ++i) plan.p.proj[i].y = ys[i];
         plan.p.x = x;
+        plan.p.xsums = form.xsums;
+        plan.p.epi = form.epi;
         CUtensorMap map;
         rc = make_x_map_decode(x, M, K, &map);
         if (rc) return rc;
-        if (launch_decode(ws[0].bits, ws[0].group, plan.p, map, plan.grid, st, exact) != cudaSuccess)
+        if (launch_decode(ws[0].bits, ws[0].group, plan.p, map, plan.grid, st, form.exact) != cudaSuccess)
             return AFFQMM_E_CUDA;
         return AFFQMM_OK;
     }
@@ -428,7 +443,32 @@ int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y
 int affqmm_run_exact(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y, void* workspace,
                      size_t ws_bytes, void* stream) {
     uint16_t* ys[1] = {y};
-    return run_impl(1, w, x, M, ys, workspace, ws_bytes, stream, true);
+    Form f;
+    f.exact = true;
+    return run_impl(1, w, x, M, ys, workspace, ws_bytes, stream, f);
+}
+
+int affqmm_run_exact_sums(const affqmm_weight* w, const uint16_t* x, const float* xsums, int64_t M, uint16_t* y,
+                          void* workspace, size_t ws_bytes, void* stream) {
+    if (M > 0 && w && w->K > 0 && !xsums) return AFFQMM_E_NULL;
+    uint16_t* ys[1] = {y};
+    Form f;
+    f.exact = true;
+    f.xsums = xsums;
+    return run_impl(1, w, x, M, ys, workspace, ws_bytes, stream, f);
+}
+
+int affqmm_run_geglu(const affqmm_weight* w, const uint16_t* x, const float* xsums, int64_t M, int form,
+                     uint16_t* h, void* workspace, size_t ws_bytes, void* stream) {
+    if (form != AFFQMM_FORM_ROUNDED && form != AFFQMM_FORM_EXACT && form != AFFQMM_FORM_EXACT_SUMS)
+        return AFFQMM_E_ARG;
+    if (form == AFFQMM_FORM_EXACT_SUMS && M > 0 && w && w->K > 0 && !xsums) return AFFQMM_E_NULL;
+    uint16_t* ys[1] = {h};
+    Form f;
+    f.exact = form != AFFQMM_FORM_ROUNDED;
+    f.xsums = form == AFFQMM_FORM_EXACT_SUMS ? xsums : nullptr;
+    f.epi = 1;
+    return run_impl(1, w, x, M, ys, workspace, ws_bytes, stream, f);
 }
 
 int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, uint16_t* const* ys,
@@ -447,7 +487,7 @@ int affqmm_run_host(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16
     if (w->K > 0 && !x) return AFFQMM_E_NULL;
     uint16_t* ys[1] = {y_dev};
     // every check of the device call (x_dev, y_dev, workspace, device) before anything is enqueued
-    rc = run_impl(1, w, x_dev, M, ys, workspace, ws_bytes, stream, false, true);
+    rc = run_impl(1, w, x_dev, M, ys, workspace, ws_bytes, stream, Form(), true);
     if (rc) return rc;
     CopyHtoDFn htod = copy_htod();
     CopyDtoHFn dtoh = copy_dtoh();

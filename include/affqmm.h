@@ -183,6 +183,46 @@ AFFQMM_API int affqmm_run(const affqmm_weight* w, const uint16_t* x, int64_t M, 
 AFFQMM_API int affqmm_run_exact(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16_t* y, void* workspace,
                                 size_t ws_bytes, void* stream);
 
+/* The exact-codes form with the group sums of x supplied by the kernel that
+ * produced x ("Gemma 4 12B on the native Metal engine" page: the norm,
+ * merge, attention-tail, geglu and dense-tail kernels write the next
+ * projection's group sums, so the lane projection runs without computing
+ * its own):
+ *     y[m, n] = bf16( sum_g ( s_g * sum_{k in g} q[n,k] x[m,k] + b_g * xsums[m, g] ) )
+ *   xsums   device, fp32 [M, K/group] row-major, 4-byte aligned: the sums of
+ *           each group of x (in whatever fixed order the producer added
+ *           them); used as given
+ * Arguments, workspace, ordering and errors as affqmm_run_exact (M <= 16),
+ * plus E_NULL for a NULL xsums when M > 0 and K > 0, and E_ALIGN. */
+AFFQMM_API int affqmm_run_exact_sums(const affqmm_weight* w, const uint16_t* x, const float* xsums, int64_t M,
+                                     uint16_t* y, void* workspace, size_t ws_bytes, void* stream);
+
+/* Forms of the decode projection for affqmm_run_geglu. */
+#define AFFQMM_FORM_ROUNDED 0     /* bf16(s*q + b) weights, as affqmm_run */
+#define AFFQMM_FORM_EXACT 1       /* exact codes, the kernel's own group sums of x, as affqmm_run_exact */
+#define AFFQMM_FORM_EXACT_SUMS 2  /* exact codes with the caller's group sums, as affqmm_run_exact_sums */
+
+/* A gate/up stack with GeGLU as its epilogue ("Gemma 4 12B on the native
+ * Metal engine" page: geglu as the gate/up projection's epilogue, the stack's
+ * rows interleaved in 16-row blocks, the same bits as apart; "cuda gemma4"
+ * page: mlx_lm's gelu_approx(gate) * up as MLX's bf16 operations).
+ *   w      the stack, N = 2F rows interleaved in 16-row blocks: rows
+ *          32j .. 32j + 15 are gate rows 16j .. 16j + 15, rows 32j + 16 ..
+ *          32j + 31 the up rows of the same hidden units; N % 32 == 0
+ *   form   AFFQMM_FORM_ROUNDED, _EXACT or _EXACT_SUMS (xsums as
+ *          affqmm_run_exact_sums; ignored otherwise)
+ *   h      device, bf16 [M, F] row-major, 2-byte aligned; fully written:
+ *              h[m, f] = gelu_approx(gate) * up,
+ *          gate and up the bf16 outputs the projection alone would store for
+ *          the two rows, and gelu_approx(g) = 0.5 g (1 + tanh(sqrt(2/pi)
+ *          (g + 0.044715 g^3))) with every operation rounded to bf16 and the
+ *          constants taken as bf16; tanh is the device's tanhf
+ * M <= 16; workspace and ordering as affqmm_run.
+ * Errors: as affqmm_run, plus E_M for M > 16, E_SHAPE for N % 32 != 0, E_ARG
+ * for an unknown form. */
+AFFQMM_API int affqmm_run_geglu(const affqmm_weight* w, const uint16_t* x, const float* xsums, int64_t M, int form,
+                                uint16_t* h, void* workspace, size_t ws_bytes, void* stream);
+
 /* Several projections of the same x in one launch: a layer's q/k/v or
  * gate/up stack ("Gemma 4 12B on the native Metal engine" page, the commit
  * that packs each layer's q/k/v, o, gate/up and down stacks and the tied
