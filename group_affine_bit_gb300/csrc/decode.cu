@@ -12,39 +12,35 @@
 // activation rows, where fp32 FMAs would cost one instruction per weight and
 // row.
 //
-// One CTA per SM works through one contiguous run of (128-row tile, 128-deep
-// block) units, numbered tile-major, from its last unit down to its first.
-// A ring of slots in shared memory holds two consecutive blocks each (one
-// bulk copy, 9 KB a block at 4 bits, group 64) and their activation tiles:
+// Each CTA (two per SM) works through one contiguous run of (128-row tile,
+// 128-deep block) units, numbered tile-major, from its last unit down to its
+// first.  A ring of slots in shared memory holds two consecutive blocks each
+// (one bulk copy, 9 KB a block at 4 bits, group 64) and their activation
+// tiles:
 //   * a weights producer thread copies the slot's blocks; an activation
 //     producer thread loads the slot's activation tiles with TMA -- M rows x
 //     136 k, 272 bytes a row so that the eight rows of a matrix load sit on
 //     distinct banks -- into tiles whose rows M..15 stay zero;
-//   * sixteen consumer warps share every slot: warps 0-7 (group A) take its
-//     upper block, warps 8-15 (group B) its lower one; consumer warp w owns
-//     rows 16(w mod 8) .. +15 of its block.  Thread t (g = t/4, class
-//     c = t mod 4) reads class c's code words of rows g and g + 8 and their
-//     scale/bias words (affqmm_format.cuh), loads the activation fragments
-//     with ldmatrix, releases the slot, and for each of the 8 16-deep steps
-//     rounds four weight pairs -- bf16(fma(s, q, b)), one rounding -- and
-//     issues one mma (two when M > 8) into fp32 registers.  Because both
-//     groups consume every slot, neither runs more than the ring's depth
-//     ahead of the other: the SM's issue slots are shared inside one CTA
-//     rather than between two CTAs of unequal priority;
+//   * eight consumer warps each own 16 rows of every block: thread t
+//     (g = t/4, class c = t mod 4) reads class c's code words of rows g and
+//     g + 8 and their scale/bias words (affqmm_format.cuh), loads the
+//     activation fragments with ldmatrix, releases the slot after its last
+//     read, and for each of the 8 16-deep steps rounds four weight pairs --
+//     bf16(fma(s, q, b)), one rounding -- and issues one mma (two when
+//     M > 8) into fp32 registers;
 //   * at the end of each tile segment (the part of a tile inside the run)
 //     every consumer warp writes its fp32 sums to a staging buffer in shared
-//     memory and goes on; an epilogue warp adds group A's and group B's sums
-//     (in that order) and stores the tile as bf16 y, or, for a tile that
-//     several runs share, publishes the run's fp32 partial and counts in on
-//     the tile's counter.  The last run to arrive adds every run's partial in
-//     run order and stores y.  Only the epilogue warp waits on global memory
-//     (a round trip to L2 is about a microsecond under full load), so the
-//     consumers never do.
+//     memory and goes on; an epilogue warp stores the tile as bf16 y, or, for
+//     a tile that several runs share, publishes the run's fp32 partial and
+//     counts in on the tile's counter.  The last run to arrive adds every
+//     run's partial in run order and stores y.  Only the epilogue warp waits
+//     on global memory (a round trip to L2 is about a microsecond under full
+//     load), so the consumers never do.
 // Runs are walked downwards, so a tile's lower runs reach it at their start
 // and the highest run reaches it at its very end: that run's epilogue finds
 // the other partials already published, adds them ahead of time and skips
 // the counter.  Same inputs, same bits, alone or stacked: the cut, the order
-// within a run (group A + group B) and the order of the merge are fixed.
+// within a run and the order of the merge are fixed.
 // The exact-codes instantiation (the pages' lane projection) puts the exact
 // codes into the A fragments and adds s * sum(q x) + b * sum(x) per group;
 // its activation warp loads the tiles itself and writes each group's sum of
@@ -72,24 +68,26 @@
 namespace affqmm {
 namespace {
 
-constexpr int D_CWARPS = 16;                  // consumer warps: group A = 0..7, group B = 8..15
+constexpr int D_CWARPS = 8;                   // consumer warp w owns rows 16w .. 16w + 15 of every block
 constexpr int D_WPROD = D_CWARPS;             // weights producer warp
 constexpr int D_XPROD = D_CWARPS + 1;         // activations producer warp
 constexpr int D_EPI = D_CWARPS + 2;           // epilogue warp
 constexpr int D_THREADS = (D_CWARPS + 3) * 32;
 constexpr uint32_t D_XROW = 272;              // bytes per activation row of a tile (128 k + 8 of padding)
 constexpr int D_SLOTS_MAX = 16;
-constexpr uint32_t D_SMEM = 227u * 1024u;     // dynamic shared memory per CTA (one CTA per SM)
-constexpr uint32_t D_BARS = 1024u;            // barriers and flags; staging, prefix and the ring follow
+constexpr int D_CTAS_PER_SM = 2;
+constexpr int D_MAXREG = 88;                  // 2 CTAs x 352 threads x 88 registers fit the SM's 64 K
+constexpr uint32_t D_SMEM = 113u * 1024u;     // dynamic shared memory per CTA (two CTAs per SM)
+constexpr uint32_t D_BARS = 1024u;            // barriers and flags; the staging buffers and the ring follow
 constexpr uint32_t D_XSUM = 256;              // per block, exact-codes mode: [4 groups][16 rows] fp32 sums of x
 
 // A ring slot: the lower block (position 0), the upper block (position 1),
 // their activation tiles in the same order, then their group sums.  The
-// upper block is group A's, the lower one group B's.
+// consumers take the upper block first (the run is walked downwards).
 struct DecSmem {
     uint64_t full[D_SLOTS_MAX];    // both producers' bytes (arrivals: 2)
-    uint64_t empty[D_SLOTS_MAX];   // every consumer warp (16)
-    uint64_t stage_full[2];        // every consumer warp has staged its sums (16)
+    uint64_t empty[D_SLOTS_MAX];   // every consumer warp (8)
+    uint64_t stage_full[2];        // every consumer warp has staged its sums (8)
     uint64_t stage_empty[2];       // the epilogue is done with the buffer (1)
     uint64_t never;                // completed by nothing: the fault_wait test hook waits on it
     int issued[2];                 // slots armed by the weights producer [0] and the activation producer [1]
@@ -100,11 +98,9 @@ static_assert(sizeof(DecSmem) <= D_BARS, "barriers fit in their area");
 template <int NB>
 constexpr uint32_t x_tile_bytes() { return 8u * NB * D_XROW; }   // 8 rows per activation block of the mma
 template <int NB>
-constexpr uint32_t stage_bytes() { return 2u * TILE_N * 8u * NB * 4u; }   // [group][128 rows][8 NB] fp32
+constexpr uint32_t stage_bytes() { return TILE_N * 8u * NB * 4u; }   // [128 rows][8 NB] fp32
 template <int NB>
-constexpr uint32_t prefix_bytes() { return TILE_N * 8u * NB * 4u; }       // [128 rows][8 NB] fp32
-template <int NB>
-constexpr uint32_t ring_offset() { return D_BARS + 2u * stage_bytes<NB>() + prefix_bytes<NB>(); }
+constexpr uint32_t ring_offset() { return D_BARS + 2u * stage_bytes<NB>(); }
 template <int BITS, int GROUP, int NB>
 constexpr uint32_t slot_bytes() {
     return 2u * (uint32_t)block_bytes(BITS, GROUP) + 2u * x_tile_bytes<NB>() + 2u * D_XSUM;
@@ -284,7 +280,7 @@ __device__ __forceinline__ void add_partial(float (&v)[8], const float* q) {
 }
 
 template <int BITS, int GROUP, int NB, bool EXACT>
-__global__ void __launch_bounds__(D_THREADS, 1)
+__global__ void __maxnreg__(D_MAXREG)
     decode_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     constexpr int BB = block_bytes(BITS, GROUP);
@@ -300,7 +296,6 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     const uint32_t sh_addr = (raw + 127u) & ~127u;
     DecSmem* sh = reinterpret_cast<DecSmem*>(smem_raw + (sh_addr - raw));
     const uint32_t stage0 = sh_addr + D_BARS;               // staging buffer b at stage0 + b * STG
-    const uint32_t prefix = stage0 + 2u * STG;              // the last segment's prefix sum of other runs
     const uint32_t ring = sh_addr + ring_offset<NB>();      // slot s at ring + s * SLOT
     const int M = p.M;
 #define BAR(field, i) (sh_addr + (uint32_t)offsetof(DecSmem, field) + 8u * (uint32_t)(i))
@@ -314,7 +309,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     const int U = P.units, PC = P.nctas, KB = p.KB;
     const int u0 = (int)((int64_t)cta * U / PC);
     const int u1 = (int)((int64_t)(cta + 1) * U / PC);
-    const int nslots = (u1 - u0 + 1) / 2;       // slot j: units u1-1-2j (upper, group A) and u1-2-2j (lower, B)
+    const int nslots = (u1 - u0 + 1) / 2;       // slot j: units u1-1-2j (upper) and u1-2-2j (lower)
     const int tile_top = (u1 - 1) / KB, tile_bot = u0 / KB;
     const int nsegs = tile_top - tile_bot + 1;  // segment k: the run's part of tile tile_top - k
 
@@ -462,9 +457,11 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             unsigned* ctr = &p.counters[P.ctr_begin + t];
             const int b = k & 1;
             // The highest run of a shared tile reaches it last: when every lower
-            // run has already published its partial, add them in run order now.
+            // run has already published its partial, add them in run order now,
+            // into the other staging buffer (free: this is the last segment).
             bool fast = false;
-            if (!whole && cta == cl && cf < cl) {
+            const uint32_t prefix = stage0 + (uint32_t)(1 - b) * STG;
+            if (!whole && k == nsegs - 1 && cta == cl && cf < cl) {
                 unsigned cnt = 0;
                 if (lane == 0) cnt = ld_acquire_gpu(ctr);
                 cnt = __shfl_sync(0xffffffffu, cnt, 0);
@@ -492,19 +489,16 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(stage_full, b), (uint32_t)((k >> 1) & 1), abort_flag,
                                                        p.status)))
                 break;
-            // this run's value of weight row 32 i + lane: group A's sums + group B's sums
+            // this run's value of weight row 32 i + lane, as the consumers staged it
             auto own = [&](int mc, int i, float (&v)[8]) {
                 const uint32_t ra = stage0 + (uint32_t)b * STG + ((uint32_t)(32 * i + lane) * MP + 8u * mc) * 4u;
-                const uint32_t rb = ra + STG / 2;
-                float a0[4], a1[4], b0[4], b1[4];
+                float a0[4], a1[4];
                 lds_v4f(ra, a0);
                 lds_v4f(ra + 16u, a1);
-                lds_v4f(rb, b0);
-                lds_v4f(rb + 16u, b1);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    v[e] = a0[e] + b0[e];
-                    v[4 + e] = a1[e] + b1[e];
+                    v[e] = a0[e];
+                    v[4 + e] = a1[e];
                 }
             };
             auto partial_of = [&](int run, int mc, int i) -> const float* {
@@ -582,11 +576,8 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         }
     } else {
         // ---------------------------------------------------------- consumers
-        const int grp = warp >> 3;                // 0: group A (upper block of each slot), 1: group B
-        const int wr = warp & 7;
-        const uint32_t pos = (uint32_t)(1 - grp);  // the block's position in the slot
         const int g = lane >> 2, c = lane & 3;
-        const int r_lo = 16 * wr + g, r_hi = r_lo + 8;  // this thread's rows within the tile
+        const int r_lo = 16 * warp + g, r_hi = r_lo + 8;  // this thread's rows within the tile
         // ldmatrix: lanes 8j .. 8j + 7 address matrix j's eight rows; matrix j
         // of a pair of steps is (step 2p + j/2, k half j mod 2)
         const uint32_t xlane = (uint32_t)(lane & 7) * D_XROW + (uint32_t)((lane >> 3) & 1) * 16u + (uint32_t)(lane >> 4) * 32u;
@@ -600,7 +591,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(stage_empty, b), (uint32_t)((k >> 1) & 1) ^ 1u, abort_flag,
                                                        p.status)))
                 return false;
-            const uint32_t base = stage0 + (uint32_t)b * STG + (uint32_t)grp * (STG / 2);
+            const uint32_t base = stage0 + (uint32_t)b * STG;
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
                 sts_v2f(base + ((uint32_t)r_lo * MP + 8u * nb + 2u * c) * 4u, acc[4 * nb + 0], acc[4 * nb + 1]);
@@ -621,40 +612,41 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         int cur = 0;  // the segment acc belongs to
         for (int j = 0; run && j < nslots; ++j) {
             const int s = j % NS;
-            const int u = u1 - 1 - 2 * j - grp;
-            if (u < u0) {  // the run's odd last slot holds group A's block only
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(empty, s));
-                break;
-            }
-            const int seg = tile_top - u / KB;
-            while (run && cur < seg) run = stage(cur++);
-            if (!run) break;
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), (uint32_t)((j / NS) & 1), abort_flag, p.status))) {
                 run = false;
                 break;
             }
             const uint32_t st = ring + (uint32_t)s * SLOT;
-            const uint32_t blk = st + pos * (uint32_t)BB;
-            uint32_t wl[BITS], wh[BITS], sl[SBW], sh2[SBW];
-            load_class_words_smem<BITS>(blk, r_lo, c, wl);
-            load_class_words_smem<BITS>(blk, r_hi, c, wh);
-            load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, r_lo), sl);
-            load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, r_hi), sh2);
-            uint32_t b[NB][8][2];
-            load_x_frags<NB>(st + 2u * BB + pos * XT + xlane, b);
-            if (!EXACT) {  // every read of the slot is issued: release it
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(empty, s));
-            }
-            if constexpr (EXACT)
-                mma_steps_exact<BITS, GROUP, NB>(wl, wh, sl, sh2, b, st + 2u * BB + 2u * XT + pos * D_XSUM, c, acc,
-                                                 accg);
-            else
-                mma_steps<BITS, GROUP, NB>(wl, wh, sl, sh2, b, acc);
-            if (EXACT) {  // the group sums are read too: release the slot
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(empty, s));
+            const int uh = u1 - 1 - 2 * j;
+            const bool two = uh - 1 >= u0;
+#pragma unroll
+            for (int h = 1; h >= 0; --h) {  // the upper block, then the lower one
+                if (h == 0 && !two) break;
+                const int u = uh - (1 - h);
+                const int seg = tile_top - u / KB;
+                while (run && cur < seg) run = stage(cur++);
+                if (!run) break;
+                const uint32_t blk = st + (uint32_t)h * (uint32_t)BB;
+                uint32_t wl[BITS], wh[BITS], sl[SBW], sh2[SBW];
+                load_class_words_smem<BITS>(blk, r_lo, c, wl);
+                load_class_words_smem<BITS>(blk, r_hi, c, wh);
+                load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, r_lo), sl);
+                load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, r_hi), sh2);
+                uint32_t b[NB][8][2];
+                load_x_frags<NB>(st + 2u * BB + (uint32_t)h * XT + xlane, b);
+                if (!EXACT && (h == 0 || !two)) {  // every read of the slot is issued: release it
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(empty, s));
+                }
+                if constexpr (EXACT)
+                    mma_steps_exact<BITS, GROUP, NB>(wl, wh, sl, sh2, b, st + 2u * BB + 2u * XT + (uint32_t)h * D_XSUM,
+                                                     c, acc, accg);
+                else
+                    mma_steps<BITS, GROUP, NB>(wl, wh, sl, sh2, b, acc);
+                if (EXACT && (h == 0 || !two)) {  // the group sums are read too: release the slot
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(empty, s));
+                }
             }
         }
         while (run && cur < nsegs) run = stage(cur++);
@@ -692,12 +684,15 @@ cudaError_t launch_b(int group, const DecParams& p, const CUtensorMap& map, int 
     return launch_bg<BITS, 128>(p, map, grid, st, exact);
 }
 
-// The kernel's shared-memory limit and how many CTAs of it an SM holds (min
-// over the instantiations, which differ only in registers).
+// The kernel's shared-memory limit, the largest shared-memory carveout (two
+// CTAs of 113 KB per SM), and how many CTAs of it an SM holds (min over the
+// instantiations, which differ only in registers).
 template <int BITS, int GROUP, int NB, bool EXACT>
 cudaError_t allow_bgn(int* per_sm) {
     auto* k = decode_kernel<BITS, GROUP, NB, EXACT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)D_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int n = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, D_THREADS, (size_t)D_SMEM);
@@ -729,7 +724,7 @@ int64_t decode_fault_wait() { return __atomic_load_n(&g_fault_wait, __ATOMIC_REL
 void decode_set_fault_wait(int64_t cycles) { __atomic_store_n(&g_fault_wait, (long long)cycles, __ATOMIC_RELAXED); }
 
 cudaError_t decode_allow_smem(int* ctas_per_sm) {
-    int n = 1;
+    int n = D_CTAS_PER_SM;
     for (cudaError_t e : {allow_b<2>(&n), allow_b<3>(&n), allow_b<4>(&n), allow_b<5>(&n), allow_b<6>(&n), allow_b<8>(&n)})
         if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
