@@ -77,7 +77,7 @@ constexpr uint32_t D_XROW = 272;              // bytes per activation row of a t
 constexpr int D_SLOTS_MAX = 16;
 constexpr int D_CTAS_PER_SM = 2;
 constexpr int D_MAXREG = 88;                  // 2 CTAs x 352 threads x 88 registers fit the SM's 64 K
-constexpr uint32_t D_SMEM = 113u * 1024u;     // dynamic shared memory per CTA (two CTAs per SM)
+constexpr uint32_t D_SMEM = 112u * 1024u;     // dynamic shared memory per CTA (two CTAs per SM)
 constexpr uint32_t D_BARS = 1024u;            // barriers and flags; the staging buffers and the ring follow
 constexpr uint32_t D_XSUM = 256;              // per block, exact-codes mode: [4 groups][16 rows] fp32 sums of x
 
@@ -685,7 +685,7 @@ cudaError_t launch_b(int group, const DecParams& p, const CUtensorMap& map, int 
 }
 
 // The kernel's shared-memory limit, the largest shared-memory carveout (two
-// CTAs of 113 KB per SM), and how many CTAs of it an SM holds (min over the
+// CTAs of 112 KB per SM), and how many CTAs of it an SM holds (min over the
 // instantiations, which differ only in registers).
 template <int BITS, int GROUP, int NB, bool EXACT>
 cudaError_t allow_bgn(int* per_sm) {
