@@ -76,7 +76,6 @@ constexpr int D_THREADS = (D_CWARPS + 3) * 32;
 constexpr uint32_t D_XROW = 272;              // bytes per activation row of a tile (128 k + 8 of padding)
 constexpr int D_SLOTS_MAX = 16;
 constexpr int D_CTAS_PER_SM = 2;
-constexpr int D_MAXREG = 88;                  // 2 CTAs x 352 threads x 88 registers fit the SM's 64 K
 constexpr uint32_t D_SMEM = 112u * 1024u;     // dynamic shared memory per CTA (two CTAs per SM)
 constexpr uint32_t D_BARS = 1024u;            // barriers and flags; the staging buffers and the ring follow
 constexpr uint32_t D_XSUM = 256;              // per block, exact-codes mode: [4 groups][16 rows] fp32 sums of x
@@ -125,6 +124,18 @@ __device__ __forceinline__ void lds_v4f(uint32_t a, float (&v)[4]) {
 __device__ __forceinline__ void sts_v4f(uint32_t a, const float (&v)[4]) {
     asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3])
                  : "memory");
+}
+// Order this thread's earlier global accesses before its later ones at GPU
+// scope (release and acquire; lighter than the sequentially consistent fence).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Whether the phase of parity `parity` of `bar` has completed (no waiting).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
 }
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
@@ -280,7 +291,7 @@ __device__ __forceinline__ void add_partial(float (&v)[8], const float* q) {
 }
 
 template <int BITS, int GROUP, int NB, bool EXACT>
-__global__ void __maxnreg__(D_MAXREG)
+__global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
     decode_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     constexpr int BB = block_bytes(BITS, GROUP);
@@ -456,34 +467,51 @@ __global__ void __maxnreg__(D_MAXREG)
             const int cf = run_of(t * KB, U, PC), cl = run_of(t * KB + KB - 1, U, PC);
             unsigned* ctr = &p.counters[P.ctr_begin + t];
             const int b = k & 1;
-            // The highest run of a shared tile reaches it last: when every lower
-            // run has already published its partial, add them in run order now,
-            // into the other staging buffer (free: this is the last segment).
+            // The highest run of a shared tile reaches it last.  While its
+            // consumers finish the run's last segment the epilogue watches the
+            // tile's counter; once every lower run has published its partial it
+            // adds them in run order, into the other staging buffer (free: this
+            // is the last segment), and this run then needs no counter at all.
             bool fast = false;
             const uint32_t prefix = stage0 + (uint32_t)(1 - b) * STG;
-            if (!whole && k == nsegs - 1 && cta == cl && cf < cl) {
+            auto all_published = [&]() -> bool {
                 unsigned cnt = 0;
                 if (lane == 0) cnt = ld_acquire_gpu(ctr);
                 cnt = __shfl_sync(0xffffffffu, cnt, 0);
-                if (cnt == (unsigned)(cl - cf)) {
-                    fast = true;
-                    __threadfence();  // every lane reads the partials after the acquire
-                    for (int mc = 0; mc < NB; ++mc)
+                return cnt == (unsigned)(cl - cf);
+            };
+            auto take_prefix = [&]() {
+                fence_acq_rel_gpu();  // every lane reads the partials after the acquire
+                for (int mc = 0; mc < NB; ++mc)
 #pragma unroll 1
-                        for (int i = 0; i < 4; ++i) {
-                            float pre[8];
+                    for (int i = 0; i < 4; ++i) {
+                        float pre[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) pre[e] = 0.f;
-                            const int r = 32 * i + lane;
-                            for (int run = cf; run < cl; ++run) {
-                                const int ub = (int)((int64_t)run * U / PC);
-                                const int sc = P.slot_begin + 2 * run + (t == ub / KB ? 0 : 1);
-                                add_partial(pre, p.partials + (size_t)sc * kDecSlotFloats + (size_t)r * 16 + 8 * mc);
-                            }
-                            const uint32_t a = prefix + ((uint32_t)r * MP + 8u * mc) * 4u;
-                            sts_v4f(a, {pre[0], pre[1], pre[2], pre[3]});
-                            sts_v4f(a + 16u, {pre[4], pre[5], pre[6], pre[7]});
+                        for (int e = 0; e < 8; ++e) pre[e] = 0.f;
+                        const int r = 32 * i + lane;
+                        for (int run = cf; run < cl; ++run) {
+                            const int ub = (int)((int64_t)run * U / PC);
+                            const int sc = P.slot_begin + 2 * run + (t == ub / KB ? 0 : 1);
+                            add_partial(pre, p.partials + (size_t)sc * kDecSlotFloats + (size_t)r * 16 + 8 * mc);
                         }
+                        const uint32_t a = prefix + ((uint32_t)r * MP + 8u * mc) * 4u;
+                        sts_v4f(a, {pre[0], pre[1], pre[2], pre[3]});
+                        sts_v4f(a + 16u, {pre[4], pre[5], pre[6], pre[7]});
+                    }
+            };
+            const bool candidate = !whole && k == nsegs - 1 && cta == cl && cf < cl;
+            if (candidate) {
+                const uint32_t par = (uint32_t)((k >> 1) & 1);
+                const long long t_start = clock64();
+                for (;;) {
+                    const bool ready = __all_sync(0xffffffffu, mbar_test(BAR(stage_full, b), par));
+                    if (all_published()) {
+                        take_prefix();
+                        fast = true;
+                        break;
+                    }
+                    if (ready || *abort_flag || clock64() - t_start > kWaitLimitCycles) break;
+                    __nanosleep(500);
                 }
             }
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(stage_full, b), (uint32_t)((k >> 1) & 1), abort_flag,
@@ -543,13 +571,13 @@ __global__ void __maxnreg__(D_MAXREG)
                         __stcg(q, make_float4(v[0], v[1], v[2], v[3]));
                         __stcg(q + 1, make_float4(v[4], v[5], v[6], v[7]));
                     }
-                __threadfence();  // every lane's partial is visible GPU-wide before the arrival
+                fence_acq_rel_gpu();  // every lane's partial is visible GPU-wide before the arrival
                 __syncwarp();
                 unsigned prev = 0;
                 if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
                 if (prev == (unsigned)(cl - cf)) {  // the last run to arrive adds every run's partial in run order
-                    __threadfence();
+                    fence_acq_rel_gpu();
                     for (int mc = 0; mc < NB; ++mc)
 #pragma unroll 1
                         for (int i = 0; i < 4; ++i) {
@@ -610,6 +638,7 @@ __global__ void __maxnreg__(D_MAXREG)
                    __all_sync(0xffffffffu,
                               wait_or_abort_within(BAR(never, 0), 0u, abort_flag, p.status, p.fault_wait));
         int cur = 0;  // the segment acc belongs to
+        int seg = 0, kbu = (u1 - 1) % KB;  // the segment and depth block of the next block (walked downwards)
         for (int j = 0; run && j < nslots; ++j) {
             const int s = j % NS;
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), (uint32_t)((j / NS) & 1), abort_flag, p.status))) {
@@ -622,8 +651,6 @@ __global__ void __maxnreg__(D_MAXREG)
 #pragma unroll
             for (int h = 1; h >= 0; --h) {  // the upper block, then the lower one
                 if (h == 0 && !two) break;
-                const int u = uh - (1 - h);
-                const int seg = tile_top - u / KB;
                 while (run && cur < seg) run = stage(cur++);
                 if (!run) break;
                 const uint32_t blk = st + (uint32_t)h * (uint32_t)BB;
@@ -646,6 +673,10 @@ __global__ void __maxnreg__(D_MAXREG)
                 if (EXACT && (h == 0 || !two)) {  // the group sums are read too: release the slot
                     __syncwarp();
                     if (lane == 0) mbar_arrive(BAR(empty, s));
+                }
+                if (--kbu < 0) {
+                    kbu = KB - 1;
+                    ++seg;
                 }
             }
         }
