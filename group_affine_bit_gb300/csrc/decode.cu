@@ -89,6 +89,7 @@ struct DecSmem {
     uint64_t stage_full[2];        // every consumer warp has staged its sums (8)
     uint64_t stage_empty[2];       // the epilogue is done with the buffer (1)
     uint64_t never;                // completed by nothing: the fault_wait test hook waits on it
+    uint64_t merge;                // the last segment's copies of other runs' partials (1)
     int issued[2];                 // slots armed by the weights producer [0] and the activation producer [1]
     int abort_flag;
 };
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
             mbar_init(BAR(stage_empty, b), 1);
         }
         mbar_init(BAR(never, 0), 1);
+        mbar_init(BAR(merge, 0), 1);
         sh->issued[0] = sh->issued[1] = 0;
         sh->abort_flag = 0;
         fence_mbar_init();
@@ -578,23 +580,72 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                 prev = __shfl_sync(0xffffffffu, prev, 0);
                 if (prev == (unsigned)(cl - cf)) {  // the last run to arrive adds every run's partial in run order
                     fence_acq_rel_gpu();
+                    // At the run's last segment the ring is free (every block has
+                    // been consumed): one bulk copy per other run lands all of
+                    // their partials in it in one round trip.  Otherwise the
+                    // partials are read run by run, all four rows of a run at once.
+                    const int cap = (int)((uint32_t)NS * SLOT / (uint32_t)(kDecSlotFloats * 4));
+                    const bool landed = k == nsegs - 1 && cl - cf <= cap;
+                    if (landed) {
+                        if (lane == 0) {
+                            asm volatile("fence.proxy.async.global;" ::: "memory");  // the acquire, then the copies' reads
+                            mbar_arrive_expect_tx(BAR(merge, 0), (uint32_t)(cl - cf) * (uint32_t)(kDecSlotFloats * 4));
+                            int slot_i = 0;
+                            for (int run = cf; run <= cl; ++run) {
+                                if (run == cta) continue;
+                                const int ub = (int)((int64_t)run * U / PC);
+                                const int sc = P.slot_begin + 2 * run + (t == ub / KB ? 0 : 1);
+                                bulk_g2s(ring + (uint32_t)slot_i++ * (uint32_t)(kDecSlotFloats * 4),
+                                         p.partials + (size_t)sc * kDecSlotFloats, (uint32_t)(kDecSlotFloats * 4),
+                                         BAR(merge, 0));
+                            }
+                        }
+                        if (!__all_sync(0xffffffffu, wait_or_abort(BAR(merge, 0), 0u, abort_flag, p.status))) break;
+                    }
                     for (int mc = 0; mc < NB; ++mc)
 #pragma unroll 1
-                        for (int i = 0; i < 4; ++i) {
-                            float v[8];
+                        for (int ih = 0; ih < 2; ++ih) {  // weight rows 32 i + lane, i = 2 ih, 2 ih + 1
+                            float v[2][8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) v[i][e] = 0.f;
+                            int slot_i = 0;
                             for (int run = cf; run <= cl; ++run) {
-                                if (run == cta) {
-                                    float mine[8];
-                                    own(mc, i, mine);
+                                // this run's partial: its own staged sums, a copy in the ring, or global memory
+                                const bool mine = run == cta;
+                                if (mine || landed) {
+                                    const uint32_t sbase = mine ? stage0 + (uint32_t)b * STG
+                                                                : ring + (uint32_t)slot_i++ * (uint32_t)(kDecSlotFloats * 4);
+                                    const uint32_t srow = mine ? (uint32_t)MP : 16u;
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) v[e] += mine[e];
+                                    for (int i = 0; i < 2; ++i) {
+                                        float a0[4], a1[4];
+                                        const uint32_t a = sbase + ((uint32_t)(32 * (2 * ih + i) + lane) * srow + 8u * mc) * 4u;
+                                        lds_v4f(a, a0);
+                                        lds_v4f(a + 16u, a1);
+#pragma unroll
+                                        for (int e = 0; e < 4; ++e) {
+                                            v[i][e] += a0[e];
+                                            v[i][4 + e] += a1[e];
+                                        }
+                                    }
                                 } else {
-                                    add_partial(v, partial_of(run, mc, i));
+                                    const int ub = (int)((int64_t)run * U / PC);
+                                    const int sc = P.slot_begin + 2 * run + (t == ub / KB ? 0 : 1);
+                                    const float4* src = reinterpret_cast<const float4*>(p.partials + (size_t)sc * kDecSlotFloats) +
+                                                        (size_t)(64 * ih + lane) * 4 + 2 * mc;
+                                    // both rows' loads first: one round trip a run
+                                    const float4 q0 = __ldcg(src), q1 = __ldcg(src + 1);
+                                    const float4 q2 = __ldcg(src + 32 * 4), q3 = __ldcg(src + 32 * 4 + 1);
+                                    v[0][0] += q0.x; v[0][1] += q0.y; v[0][2] += q0.z; v[0][3] += q0.w;
+                                    v[0][4] += q1.x; v[0][5] += q1.y; v[0][6] += q1.z; v[0][7] += q1.w;
+                                    v[1][0] += q2.x; v[1][1] += q2.y; v[1][2] += q2.z; v[1][3] += q2.w;
+                                    v[1][4] += q3.x; v[1][5] += q3.y; v[1][6] += q3.z; v[1][7] += q3.w;
                                 }
                             }
-                            store_row_chunk(p, P, t, mc, i, lane, v);
+                            store_row_chunk(p, P, t, mc, 2 * ih, lane, v[0]);
+                            store_row_chunk(p, P, t, mc, 2 * ih + 1, lane, v[1]);
                         }
                     if (lane == 0) *ctr = 0u;
                 }
