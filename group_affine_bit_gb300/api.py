@@ -15,7 +15,7 @@ from dataclasses import dataclass, field
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libaffqmm.so")
+LIB_PATH = os.environ.get("AFFQMM_LIB_PATH") or os.path.join(_PKG, "libaffqmm.so")   # the in-tree build unless overridden
 
 MAX_STACK = 8
 MAX_M = 1 << 20

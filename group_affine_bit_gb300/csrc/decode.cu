@@ -68,15 +68,24 @@
 namespace affqmm {
 namespace {
 
-constexpr int D_CWARPS = 8;                   // consumer warp w owns rows 16w .. 16w + 15 of every block
+// Consumer groups per CTA.  1: two CTAs per SM, eight consumer warps each,
+// every warp taking both blocks of a slot.  2: one CTA per SM, sixteen
+// consumer warps; group 0 takes the upper block of each slot, group 1 the
+// lower one, and the epilogue adds the groups' sums in that order.
+#ifndef AFFQMM_DECODE_GROUPS
+#define AFFQMM_DECODE_GROUPS 1
+#endif
+constexpr int D_GROUPS = AFFQMM_DECODE_GROUPS;
+static_assert(D_GROUPS == 1 || D_GROUPS == 2, "one or two consumer groups");
+constexpr int D_CWARPS = 8 * D_GROUPS;        // consumer warp w owns rows 16 (w mod 8) .. + 15 of its blocks
 constexpr int D_WPROD = D_CWARPS;             // weights producer warp
 constexpr int D_XPROD = D_CWARPS + 1;         // activations producer warp
 constexpr int D_EPI = D_CWARPS + 2;           // epilogue warp
 constexpr int D_THREADS = (D_CWARPS + 3) * 32;
 constexpr uint32_t D_XROW = 272;              // bytes per activation row of a tile (128 k + 8 of padding)
 constexpr int D_SLOTS_MAX = 16;
-constexpr int D_CTAS_PER_SM = 2;
-constexpr uint32_t D_SMEM = 112u * 1024u;     // dynamic shared memory per CTA (two CTAs per SM)
+constexpr int D_CTAS_PER_SM = D_GROUPS == 1 ? 2 : 1;
+constexpr uint32_t D_SMEM = D_GROUPS == 1 ? 112u * 1024u : 227u * 1024u;   // dynamic shared memory per CTA
 constexpr uint32_t D_BARS = 1024u;            // barriers and flags; the staging buffers and the ring follow
 constexpr uint32_t D_XSUM = 256;              // per block, exact-codes mode: [4 groups][16 rows] fp32 sums of x
 
@@ -98,7 +107,7 @@ static_assert(sizeof(DecSmem) <= D_BARS, "barriers fit in their area");
 template <int NB>
 constexpr uint32_t x_tile_bytes() { return 8u * NB * D_XROW; }   // 8 rows per activation block of the mma
 template <int NB>
-constexpr uint32_t stage_bytes() { return TILE_N * 8u * NB * 4u; }   // [128 rows][8 NB] fp32
+constexpr uint32_t stage_bytes() { return D_GROUPS * TILE_N * 8u * NB * 4u; }   // [group][128 rows][8 NB] fp32
 template <int NB>
 constexpr uint32_t ring_offset() { return D_BARS + 2u * stage_bytes<NB>(); }
 template <int BITS, int GROUP, int NB>
@@ -521,14 +530,20 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                 break;
             // this run's value of weight row 32 i + lane, as the consumers staged it
             auto own = [&](int mc, int i, float (&v)[8]) {
-                const uint32_t ra = stage0 + (uint32_t)b * STG + ((uint32_t)(32 * i + lane) * MP + 8u * mc) * 4u;
-                float a0[4], a1[4];
-                lds_v4f(ra, a0);
-                lds_v4f(ra + 16u, a1);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[e] = a0[e];
-                    v[4 + e] = a1[e];
+                for (int e = 0; e < 8; ++e) v[e] = 0.f;
+#pragma unroll
+                for (int gr = 0; gr < D_GROUPS; ++gr) {  // group 0's sums, then group 1's
+                    const uint32_t ra = stage0 + (uint32_t)b * STG + (uint32_t)gr * (STG / D_GROUPS) +
+                                        ((uint32_t)(32 * i + lane) * MP + 8u * mc) * 4u;
+                    float a0[4], a1[4];
+                    lds_v4f(ra, a0);
+                    lds_v4f(ra + 16u, a1);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[e] += a0[e];
+                        v[4 + e] += a1[e];
+                    }
                 }
             };
             auto partial_of = [&](int run, int mc, int i) -> const float* {
@@ -614,14 +629,20 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                             for (int run = cf; run <= cl; ++run) {
                                 // this run's partial: its own staged sums, a copy in the ring, or global memory
                                 const bool mine = run == cta;
-                                if (mine || landed) {
-                                    const uint32_t sbase = mine ? stage0 + (uint32_t)b * STG
-                                                                : ring + (uint32_t)slot_i++ * (uint32_t)(kDecSlotFloats * 4);
-                                    const uint32_t srow = mine ? (uint32_t)MP : 16u;
+                                if (mine) {
+#pragma unroll
+                                    for (int i = 0; i < 2; ++i) {
+                                        float o[8];
+                                        own(mc, 2 * ih + i, o);
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e) v[i][e] += o[e];
+                                    }
+                                } else if (landed) {
+                                    const uint32_t sbase = ring + (uint32_t)slot_i++ * (uint32_t)(kDecSlotFloats * 4);
 #pragma unroll
                                     for (int i = 0; i < 2; ++i) {
                                         float a0[4], a1[4];
-                                        const uint32_t a = sbase + ((uint32_t)(32 * (2 * ih + i) + lane) * srow + 8u * mc) * 4u;
+                                        const uint32_t a = sbase + ((uint32_t)(32 * (2 * ih + i) + lane) * 16u + 8u * mc) * 4u;
                                         lds_v4f(a, a0);
                                         lds_v4f(a + 16u, a1);
 #pragma unroll
@@ -655,8 +676,9 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
         }
     } else {
         // ---------------------------------------------------------- consumers
+        const int grp = warp >> 3;                 // this warp's consumer group
         const int g = lane >> 2, c = lane & 3;
-        const int r_lo = 16 * warp + g, r_hi = r_lo + 8;  // this thread's rows within the tile
+        const int r_lo = 16 * (warp & 7) + g, r_hi = r_lo + 8;  // this thread's rows within the tile
         // ldmatrix: lanes 8j .. 8j + 7 address matrix j's eight rows; matrix j
         // of a pair of steps is (step 2p + j/2, k half j mod 2)
         const uint32_t xlane = (uint32_t)(lane & 7) * D_XROW + (uint32_t)((lane >> 3) & 1) * 16u + (uint32_t)(lane >> 4) * 32u;
@@ -670,7 +692,7 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(stage_empty, b), (uint32_t)((k >> 1) & 1) ^ 1u, abort_flag,
                                                        p.status)))
                 return false;
-            const uint32_t base = stage0 + (uint32_t)b * STG;
+            const uint32_t base = stage0 + (uint32_t)b * STG + (uint32_t)grp * (STG / D_GROUPS);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
                 sts_v2f(base + ((uint32_t)r_lo * MP + 8u * nb + 2u * c) * 4u, acc[4 * nb + 0], acc[4 * nb + 1]);
@@ -689,7 +711,9 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                    __all_sync(0xffffffffu,
                               wait_or_abort_within(BAR(never, 0), 0u, abort_flag, p.status, p.fault_wait));
         int cur = 0;  // the segment acc belongs to
-        int seg = 0, kbu = (u1 - 1) % KB;  // the segment and depth block of the next block (walked downwards)
+        // the segment and depth block of this warp's next block (walked downwards)
+        const int ufirst = max(u1 - 1 - (D_GROUPS == 2 ? grp : 0), u0);
+        int seg = tile_top - ufirst / KB, kbu = ufirst % KB;
         for (int j = 0; run && j < nslots; ++j) {
             const int s = j % NS;
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), (uint32_t)((j / NS) & 1), abort_flag, p.status))) {
@@ -701,7 +725,14 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
             const bool two = uh - 1 >= u0;
 #pragma unroll
             for (int h = 1; h >= 0; --h) {  // the upper block, then the lower one
-                if (h == 0 && !two) break;
+                if (D_GROUPS == 2 && h != 1 - grp) continue;  // each group its own block
+                if (h == 0 && !two) {
+                    if (D_GROUPS == 2) {  // group 1 has no block in the run's odd last slot
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(BAR(empty, s));
+                    }
+                    break;
+                }
                 while (run && cur < seg) run = stage(cur++);
                 if (!run) break;
                 const uint32_t blk = st + (uint32_t)h * (uint32_t)BB;
@@ -712,7 +743,7 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                 load_row_sb_smem<GROUP>(blk + sb_offset(BITS, GROUP, r_hi), sh2);
                 uint32_t b[NB][8][2];
                 load_x_frags<NB>(st + 2u * BB + (uint32_t)h * XT + xlane, b);
-                if (!EXACT && (h == 0 || !two)) {  // every read of the slot is issued: release it
+                if (!EXACT && (D_GROUPS == 2 || h == 0 || !two)) {  // every read of the slot is issued: release it
                     __syncwarp();
                     if (lane == 0) mbar_arrive(BAR(empty, s));
                 }
@@ -721,12 +752,13 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                                                      c, acc, accg);
                 else
                     mma_steps<BITS, GROUP, NB>(wl, wh, sl, sh2, b, acc);
-                if (EXACT && (h == 0 || !two)) {  // the group sums are read too: release the slot
+                if (EXACT && (D_GROUPS == 2 || h == 0 || !two)) {  // the group sums are read too: release the slot
                     __syncwarp();
                     if (lane == 0) mbar_arrive(BAR(empty, s));
                 }
-                if (--kbu < 0) {
-                    kbu = KB - 1;
+                kbu -= D_GROUPS;
+                while (kbu < 0) {
+                    kbu += KB;
                     ++seg;
                 }
             }
