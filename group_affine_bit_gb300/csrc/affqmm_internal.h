@@ -14,9 +14,9 @@ namespace affqmm {
 
 // One projection of a decode (M <= 16) launch: its units are
 // (128-row tile, 128-deep block) pairs, numbered tile-major (the order they
-// sit in memory), cut into `nctas` contiguous runs, one per CTA (one CTA per
-// SM).  The cut depends only on the projection, M and the device, never on
-// what else shares the launch.
+// sit in memory), cut into `nctas` contiguous runs, one per CTA.  The cut
+// depends only on the projection, M and the device, never on what else
+// shares the launch.
 struct DecProj {
     const uint8_t* packed;
     uint16_t* y;
@@ -25,7 +25,7 @@ struct DecProj {
     int32_t units;        // tiles * k-blocks
     int32_t nctas;        // CTAs working on this projection (<= units)
     int32_t cta_begin;    // first CTA of this projection in the grid
-    int32_t ctr_begin;    // first tile of this projection's merge counters (one per tile)
+    int32_t ctr_begin;    // first tile of this projection's merge counters (eight per tile)
     int32_t slot_begin;   // first partial slot (two per CTA)
 };
 
@@ -45,7 +45,7 @@ struct DecParams {
 };
 
 constexpr size_t kDecSlotFloats = 128 * 16;
-constexpr int kDecCountersPerTile = 1;
+constexpr int kDecCountersPerTile = 8;   // one per 16-row group of a tile
 
 // Workspace layout shared by every kernel: a status word, then a fixed region
 // of merge counters (zero between calls: the last user of a counter resets
