@@ -67,7 +67,9 @@ constexpr int D_CTAS_PER_SM = 2;
 constexpr uint32_t D_XROW = 272;              // bytes per activation row of a tile (128 k + 8 of padding)
 constexpr int D_SLOTS_MAX = 16;
 constexpr uint32_t D_SMEM = 110u * 1024u;     // dynamic shared memory per CTA
-constexpr uint32_t D_RING0 = 1024u;           // the ring starts here; the barriers sit below
+constexpr uint32_t D_XCHG0 = 1024u;           // the GeGLU pair exchange area starts here; the barriers sit below
+constexpr uint32_t D_XCHG_PAIR = 32u * 8u * 4u;  // one warp's sums: 32 lanes x up to 8 fp32
+constexpr uint32_t D_RING0 = D_XCHG0 + 4u * D_XCHG_PAIR;   // the ring starts here
 
 // A ring slot holds two consecutive blocks of the run (contiguous in memory:
 // one bulk copy) and their two activation tiles.  Its full barrier waits for
@@ -76,10 +78,12 @@ struct DecSmem {
     uint64_t full[D_SLOTS_MAX];
     uint64_t empty[D_SLOTS_MAX];
     uint64_t never;      // completed by nothing: the fault_wait test hook waits on it
+    uint64_t xfull[4];   // GeGLU: warp 2i + 1 has put its up sums of a whole tile in the exchange area (1)
+    uint64_t xempty[4];  // GeGLU: warp 2i has read them (1)
     int issued[2];       // slots armed by the weights producer [0] and the activation producer [1]
     int abort_flag;
 };
-static_assert(sizeof(DecSmem) <= D_RING0, "barriers fit below the ring");
+static_assert(sizeof(DecSmem) <= D_XCHG0, "barriers fit below the exchange area");
 
 template <int NB>
 constexpr uint32_t x_tile_bytes() { return 8u * NB * D_XROW; }  // 8 rows per activation block of the mma
@@ -261,10 +265,46 @@ __device__ __forceinline__ void add_runs(const DecParams& p, const DecProj& P, i
 template <int NB>
 __device__ __forceinline__ void segment_end(const DecParams& p, const DecProj& P, float* acc, int tile, bool whole,
                                             bool first_seg, int cta, int U, int PC, int KB, int M, int warp,
-                                            int lane, int r_lo, int c) {
+                                            int lane, int r_lo, int c, uint32_t xchg, uint32_t xfull,
+                                            uint32_t xempty, int& nxchg, volatile int* abort_flag) {
     const int r_hi = r_lo + 8;
     const int64_t n_lo = (int64_t)tile * TILE_N + r_lo;
     const bool geglu = p.epi != 0;
+    if (whole && geglu) {
+        // The pair's sums of a whole tile meet in shared memory: warp 2i + 1
+        // (up rows) puts its sums there, warp 2i (gate rows, the same lanes)
+        // takes them and stores h.
+        const uint32_t a = xchg + (uint32_t)lane * 32u;
+        const uint32_t ph = (uint32_t)(nxchg++ & 1);
+        if (warp & 1) {
+            if (!__all_sync(0xffffffffu, wait_or_abort(xempty, ph ^ 1u, abort_flag, p.status))) return;
+#pragma unroll
+            for (int e = 0; e < 4 * NB; ++e)
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(a + 4u * e), "f"(acc[e]) : "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xfull);
+        } else {
+            if (!__all_sync(0xffffffffu, wait_or_abort(xfull, ph, abort_flag, p.status))) return;
+            float up[4 * NB];
+#pragma unroll
+            for (int e = 0; e < 4 * NB; ++e) {
+                uint32_t v;
+                lds_v1(a + 4u * e, v);
+                up[e] = __uint_as_float(v);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xempty);
+            const int64_t F = P.N / 2;
+#pragma unroll
+            for (int e = 0; e < 4 * NB; ++e) {
+                const int m = acc_m(e, c);
+                const int64_t n = n_lo + ((e & 2) ? 8 : 0);   // a gate row: 32 j + (0 .. 15)
+                if (m < M && n < P.N)
+                    P.y[(int64_t)m * F + 16 * (n / 32) + (n % 32)] = geglu_bf16(bf16r(acc[e]), bf16r(up[e]));
+            }
+        }
+        return;
+    }
     if (whole && !geglu) {
 #pragma unroll
         for (int e = 0; e < 4 * NB; ++e) {
@@ -368,6 +408,10 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
             mbar_init(BAR(empty, s), D_CWARPS);  // every consumer warp
         }
         mbar_init(BAR(never, 0), 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(BAR(xfull, i), 1);
+            mbar_init(BAR(xempty, i), 1);
+        }
         sh->issued[0] = sh->issued[1] = 0;
         sh->abort_flag = 0;
         fence_mbar_init();
@@ -504,6 +548,7 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                          __all_sync(0xffffffffu, wait_or_abort_within(BAR(never, 0), 0u, abort_flag, p.status,
                                                                       p.fault_wait));
         int kb = u0 % KB, tile = u0 / KB, seg_start = u0;
+        int nxchg = 0;  // whole tiles exchanged through shared memory (GeGLU form)
         for (int j = 0; run && j < npairs; ++j) {
             const int s = j % NS;
             if (!__all_sync(0xffffffffu, wait_or_abort(BAR(full, s), (uint32_t)((j / NS) & 1), abort_flag, p.status)))
@@ -537,7 +582,9 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                 const int u = u0 + 2 * j + h;
                 if (kb == KB - 1 || u == u1 - 1) {  // this block ends a tile segment
                     segment_end<NB>(p, P, acc, tile, (seg_start == tile * KB) && (kb == KB - 1), seg_start == u0, cta,
-                                    U, PC, KB, M, warp, lane, r_lo, c);
+                                    U, PC, KB, M, warp, lane, r_lo, c,
+                                    sh_addr + D_XCHG0 + (uint32_t)(warp >> 1) * D_XCHG_PAIR, BAR(xfull, warp >> 1),
+                                    BAR(xempty, warp >> 1), nxchg, abort_flag);
 #pragma unroll
                     for (int e = 0; e < 4 * NB; ++e) acc[e] = 0.f;
                     seg_start = u + 1;
