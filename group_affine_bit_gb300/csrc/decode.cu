@@ -119,6 +119,11 @@ __device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uin
 // Order this thread's earlier global accesses before its later ones at GPU
 // scope (release and acquire; lighter than the sequentially consistent fence).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 // bf16 rounding of an fp32 value, back in fp32.
 __device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
@@ -314,6 +319,35 @@ __device__ __forceinline__ void segment_end(const DecParams& p, const DecProj& P
         }
         return;
     }
+    const int t0 = tile * KB, t1 = t0 + KB - 1;
+    const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
+    // A run reaches the tile that begins inside it only at its very end, while
+    // the later runs of that tile had it at their start: when they have all
+    // counted in already, this warp adds their partials and its own at once,
+    // without publishing its own or counting in.
+    if (!geglu && !whole && cta == cf && cf < cl && t1 > (int)((int64_t)(cta + 1) * U / PC) - 1) {
+        unsigned* ctr_f = &p.counters[(size_t)(P.ctr_begin + tile) * D_CWARPS + warp];
+        unsigned cnt = 0;
+        if (lane == 0) cnt = ld_acquire_gpu(ctr_f);
+        cnt = __shfl_sync(0xffffffffu, cnt, 0);
+        if (cnt == (unsigned)(cl - cf)) {
+            fence_acq_rel_gpu();
+            int rows[4 * NB];
+#pragma unroll
+            for (int e = 0; e < 4 * NB; ++e) rows[e] = (e & 2) ? r_hi : r_lo;
+            float sum[4 * NB];
+            add_runs<NB>(p, P, t0, cf, cl, U, PC, cta, acc, rows, M, c, sum);
+#pragma unroll
+            for (int e = 0; e < 4 * NB; ++e) {
+                const int m = acc_m(e, c);
+                const int64_t n = n_lo + ((e & 2) ? 8 : 0);
+                if (m < M && n < P.N) P.y[(int64_t)m * P.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum[e]));
+            }
+            __syncwarp();
+            if (lane == 0) *ctr_f = 0u;
+            return;
+        }
+    }
     const int slot = P.slot_begin + 2 * cta + (first_seg ? 0 : 1);
     float* sp = p.partials + (size_t)slot * kDecSlotFloats;
 #pragma unroll
@@ -329,8 +363,6 @@ __device__ __forceinline__ void segment_end(const DecParams& p, const DecProj& P
     unsigned* ctr = &p.counters[(size_t)(P.ctr_begin + tile) * D_CWARPS + cw];
     if (lane == 0) prev = atom_add_acq_rel(ctr, 1u);
     prev = __shfl_sync(0xffffffffu, prev, 0);
-    const int t0 = tile * KB, t1 = t0 + KB - 1;
-    const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
     const unsigned arrivals = (unsigned)(cl - cf + 1) * (geglu ? 2u : 1u);
     if (prev != arrivals - 1u) return;
     fence_acq_rel_gpu();  // the last arrival: every lane reads the other runs' partials after it
