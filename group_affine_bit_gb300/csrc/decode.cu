@@ -171,14 +171,16 @@ __device__ __forceinline__ void mma_steps(const uint32_t* wl, const uint32_t* wh
 }
 // Exact-codes mode (the pages' lane projection): the A fragment holds the
 // exact codes q (no rounding of s*q + b), the mmas of one group accumulate
-// sum_k q x in accg, and at the group's end
-//     acc += s_row * accg + b_row * sum_{k in group} x[m, k]
-// with the group sums xs (fp32 [group][16 rows]) written by the activation
-// producer.  sl/sh hold the rows' s | b << 16 words.
+// sum_k q x in accg and, against an A fragment of ones, sum_k x in accx (the
+// same value in every weight row), and at the group's end
+//     acc += s_row * accg + b_row * (sum of x over the group)
+// with the sum of x from accx, or, when the kernel that produced x wrote the
+// sums (given), from xs (fp32 [group][16 rows] in the slot).  sl/sh hold the
+// rows' s | b << 16 words.
 template <int BITS, int GROUP, int NB, int S = 0>
 __device__ __forceinline__ void mma_steps_exact(const uint32_t* wl, const uint32_t* wh, const uint32_t* sl,
-                                                const uint32_t* sh, const uint32_t (&b)[NB][8][2], uint32_t xs, int c,
-                                                float* acc, float* accg) {
+                                                const uint32_t* sh, const uint32_t (&b)[NB][8][2], uint32_t xs,
+                                                bool given, int c, float* acc, float* accg, float* accx) {
     if constexpr (S < 8) {
         constexpr int P0 = plane0_bits(BITS);
         const uint32_t a0 = class_code_pair<BITS, 2 * S>(wl, wl + P0);
@@ -186,7 +188,10 @@ __device__ __forceinline__ void mma_steps_exact(const uint32_t* wl, const uint32
         const uint32_t a2 = class_code_pair<BITS, 2 * S + 1>(wl, wl + P0);
         const uint32_t a3 = class_code_pair<BITS, 2 * S + 1>(wh, wh + P0);
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) mma_bf16(accg + 4 * nb, a0, a1, a2, a3, b[nb][S][0], b[nb][S][1]);
+        for (int nb = 0; nb < NB; ++nb) {
+            mma_bf16(accg + 4 * nb, a0, a1, a2, a3, b[nb][S][0], b[nb][S][1]);
+            mma_bf16(accx + 4 * nb, BF2_ONE, BF2_ONE, BF2_ONE, BF2_ONE, b[nb][S][0], b[nb][S][1]);
+        }
         constexpr int SPG = GROUP / 16;  // 16-deep steps per group
         if constexpr ((S + 1) % SPG == 0) {
             constexpr int GI = S / SPG;
@@ -194,9 +199,13 @@ __device__ __forceinline__ void mma_steps_exact(const uint32_t* wl, const uint32
             const float s_hi = __uint_as_float(sh[GI] << 16), b_hi = __uint_as_float(sh[GI] & 0xFFFF0000u);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-                uint32_t x0u, x1u;  // the group sums of activation rows 8nb + 2c, 8nb + 2c + 1
-                lds_v2(xs + (uint32_t)(GI * 16 + 8 * nb + 2 * c) * 4u, x0u, x1u);
-                const float x0 = __uint_as_float(x0u), x1 = __uint_as_float(x1u);
+                float x0 = accx[4 * nb], x1 = accx[4 * nb + 1];  // activation rows 8nb + 2c, 8nb + 2c + 1
+                if (given) {
+                    uint32_t x0u, x1u;
+                    lds_v2(xs + (uint32_t)(GI * 16 + 8 * nb + 2 * c) * 4u, x0u, x1u);
+                    x0 = __uint_as_float(x0u);
+                    x1 = __uint_as_float(x1u);
+                }
                 float* a = acc + 4 * nb;
                 float* q = accg + 4 * nb;
                 a[0] = fmaf(b_lo, x0, fmaf(s_lo, q[0], a[0]));
@@ -204,10 +213,21 @@ __device__ __forceinline__ void mma_steps_exact(const uint32_t* wl, const uint32
                 a[2] = fmaf(b_hi, x0, fmaf(s_hi, q[2], a[2]));
                 a[3] = fmaf(b_hi, x1, fmaf(s_hi, q[3], a[3]));
                 q[0] = q[1] = q[2] = q[3] = 0.f;
+                accx[4 * nb] = accx[4 * nb + 1] = accx[4 * nb + 2] = accx[4 * nb + 3] = 0.f;
             }
         }
-        mma_steps_exact<BITS, GROUP, NB, S + 1>(wl, wh, sl, sh, b, xs, c, acc, accg);
+        mma_steps_exact<BITS, GROUP, NB, S + 1>(wl, wh, sl, sh, b, xs, given, c, acc, accg, accx);
     }
+}
+
+// 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on `bar` once every earlier cp.async of this thread has completed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // The activation fragments of one block: 8 steps x (k low, k high) for each
@@ -436,7 +456,7 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(BAR(full, s), 2);          // both producers
+            mbar_init(BAR(full, s), (EXACT && p.xsums != nullptr) ? 3 : 2);  // both producers (and the sums' copies)
             mbar_init(BAR(empty, s), D_CWARPS);  // every consumer warp
         }
         mbar_init(BAR(never, 0), 1);
@@ -459,7 +479,7 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
     volatile int* abort_flag = &sh->abort_flag;
     if (threadIdx.x == 0) pdl_launch_dependents();
 
-    if (warp == D_WPROD || (warp == D_XPROD && !EXACT)) {
+    if (warp == D_WPROD || warp == D_XPROD) {
         // ---------------------------------------------------------- producers
         // The weights never depend on an earlier kernel, so their producer
         // starts before the grid dependency is resolved; the activations may
@@ -486,81 +506,27 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                     for (int h = 0; h < nb2; ++h)
                         tma_load_2d(st + 2u * BB + (uint32_t)h * XT, &xmap, ((u0 + 2 * j + h) % KB) * KBLK, 0,
                                     BAR(full, s));
+                    if (EXACT && p.xsums != nullptr) {
+                        // the group sums of x that x's producer wrote, 4 bytes each, into the
+                        // blocks' sum areas ([group][16 rows]); past K the copies fill zeros
+                        constexpr int GPB = KBLK / GROUP;
+                        const int64_t G = p.K / GROUP;
+                        for (int h = 0; h < nb2; ++h) {
+                            const int64_t g0 = (int64_t)((u0 + 2 * j + h) % KB) * GPB;
+                            const uint32_t sums = st + 2u * BB + 2u * XT + (uint32_t)h * D_XSUM;
+                            for (int gi = 0; gi < GPB; ++gi)
+                                for (int m = 0; m < M; ++m) {
+                                    const bool in = g0 + gi < G;
+                                    cp_async_4(sums + (uint32_t)(gi * 16 + m) * 4u,
+                                               in ? p.xsums + (int64_t)m * G + g0 + gi : p.xsums, in ? 4u : 0u);
+                                }
+                        }
+                        cp_async_arrive_noinc(BAR(full, s));  // arrives once these copies have landed
+                    }
                 }
                 issued = j + 1;
             }
             sh->issued[wprod ? 0 : 1] = issued;
-        }
-    } else if (warp == D_XPROD) {
-        // ------------------------- activations and their group sums (exact-codes mode)
-        // The whole warp loads each block's M rows of x (lane l: k = 4l .. 4l + 3),
-        // stores them in the tile layout, and adds each group's values (the
-        // lanes of a group reduce in a fixed tree) into the slot's sums.
-        pdl_wait();  // x may come from the previous kernel
-        constexpr int LPG = GROUP / 4;  // lanes per group
-        constexpr int GPB = KBLK / GROUP;
-        const int64_t G = p.K / GROUP;
-        for (int j = 0; j < npairs; ++j) {
-            const int s = j % NS;
-            int okw = 1;
-            if (lane == 0) okw = wait_or_abort_lazy(BAR(empty, s), (uint32_t)((j / NS) & 1) ^ 1u, abort_flag, p.status);
-            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-            const int nb2 = min(2, nblk - 2 * j);
-            const uint32_t st = ring + (uint32_t)s * SLOT;
-            // both blocks' loads first (one round trip to L2 per slot), then the stores and sums
-            uint32_t xw[2][8 * NB][2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int64_t k0 = (int64_t)((u0 + 2 * j + h) % KB) * KBLK + 4 * lane;
-                const bool in = h < nb2 && k0 < p.K;  // K is a multiple of 32: a lane's four values are all in or out
-#pragma unroll
-                for (int m = 0; m < 8 * NB; ++m) {
-                    xw[h][m][0] = xw[h][m][1] = 0u;
-                    if (m < M && in) {
-                        const uint2 v = __ldg(reinterpret_cast<const uint2*>(p.x + (int64_t)m * p.K + k0));
-                        xw[h][m][0] = v.x;
-                        xw[h][m][1] = v.y;
-                    }
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (h >= nb2) break;
-                const uint32_t tile = st + 2u * BB + (uint32_t)h * XT;
-                const uint32_t sums = st + 2u * BB + 2u * XT + (uint32_t)h * D_XSUM;
-#pragma unroll
-                for (int m = 0; m < 8 * NB; ++m) {
-                    if (m >= M) break;
-                    asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(tile + (uint32_t)m * D_XROW + 8u * lane),
-                                 "r"(xw[h][m][0]), "r"(xw[h][m][1])
-                                 : "memory");
-                    if (p.xsums == nullptr) {
-                        float v = __uint_as_float(xw[h][m][0] << 16) + __uint_as_float(xw[h][m][0] & 0xFFFF0000u) +
-                                  __uint_as_float(xw[h][m][1] << 16) + __uint_as_float(xw[h][m][1] & 0xFFFF0000u);
-#pragma unroll
-                        for (int off = 1; off < LPG; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                        if (lane % LPG == 0)
-                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sums + (uint32_t)((lane / LPG) * 16 + m) * 4u),
-                                         "f"(v)
-                                         : "memory");
-                    }
-                }
-                if (p.xsums != nullptr) {  // the producer's sums of this block's groups, as given
-                    const int kbh = (u0 + 2 * j + h) % KB;
-                    for (int i = lane; i < GPB * M; i += 32) {
-                        const int gi = i / M, m = i - gi * M;
-                        const int64_t gg = (int64_t)kbh * GPB + gi;
-                        const float v = gg < G ? __ldg(p.xsums + (int64_t)m * G + gg) : 0.f;
-                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sums + (uint32_t)(gi * 16 + m) * 4u), "f"(v)
-                                     : "memory");
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(BAR(full, s));  // the tiles and sums are written
-                sh->issued[1] = j + 1;
-            }
         }
     } else {
         // ---------------------------------------------------------- consumers
@@ -569,9 +535,11 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
         // ldmatrix: lanes 8j .. 8j + 7 address matrix j's eight rows; matrix j
         // of a pair of steps is (step 2p + j/2, k half j mod 2)
         const uint32_t xlane = (uint32_t)(lane & 7) * D_XROW + (uint32_t)((lane >> 3) & 1) * 16u + (uint32_t)(lane >> 4) * 32u;
-        float acc[4 * NB], accg[4 * NB];  // accg: the current group's sum of q x (exact-codes mode)
+        // exact-codes mode: accg the current group's sum of q x, accx its sum of x
+        float acc[4 * NB], accg[4 * NB], accx[4 * NB];
 #pragma unroll
-        for (int e = 0; e < 4 * NB; ++e) acc[e] = accg[e] = 0.f;
+        for (int e = 0; e < 4 * NB; ++e) acc[e] = accg[e] = accx[e] = 0.f;
+        const bool given = p.xsums != nullptr;
         pdl_wait();  // y, the partials and the counters may still be in use by the previous kernel
         // Test hook: wait, bounded by p.fault_wait cycles, on a barrier that
         // nothing completes; the wait runs out, sets the status word and the
@@ -603,8 +571,8 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
                     if (lane == 0) mbar_arrive(BAR(empty, s));
                 }
                 if constexpr (EXACT)
-                    mma_steps_exact<BITS, GROUP, NB>(wl, wh, sl, sh2, b, st + 2u * BB + 2u * XT + (uint32_t)h * D_XSUM, c,
-                                                     acc, accg);
+                    mma_steps_exact<BITS, GROUP, NB>(wl, wh, sl, sh2, b, st + 2u * BB + 2u * XT + (uint32_t)h * D_XSUM,
+                                                     given, c, acc, accg, accx);
                 else
                     mma_steps<BITS, GROUP, NB>(wl, wh, sl, sh2, b, acc);
                 if (EXACT && (h == 1 || !pair)) {  // the group sums are read too: release the slot
