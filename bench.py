@@ -12,6 +12,8 @@ over one batch of synthetic input with the weights resident in HBM:
   lane_sweep                M in {2,4,8,16} at 4-bit g64 and M=16 at 8b/3b/2b
   tiny                      M=1, K=256, N=512, 4-bit g64
   embed_rows                4096 scaled embedding rows gathered from the tied head's table
+                            (its row-contiguous copy)
+  embed_rows_blocks         the same gather read from the packed blocks themselves
 
 `value` is packed-weight bytes (codes + bf16 scales + biases) per second for
 the decode workloads and TFLOP/s for the prompt chunk.  Weight copies rotate
@@ -58,7 +60,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="gate_up_decode",
                     choices=["gate_up_decode", "decode_step", "prompt_chunk", "lane_sweep", "tiny", "embed_rows",
-                             "gate_up_exact"])
+                             "embed_rows_blocks", "gate_up_exact"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -247,8 +249,9 @@ class Case:
 
     @property
     def kernels(self) -> int:
-        """All of the library's kernel launches: a prompt chunk also launches its merge kernel."""
-        return 1 if self.M <= 16 else 2 * (-(-self.M // 128))
+        """All of the library's kernel launches (one per 128-row chunk; the
+        split-depth merge runs inside the projection kernel)."""
+        return self.launches
 
     def oracle_shape(self):
         return dict(bits=self.bits, group=self.group, M=self.M, N=self.N, K=self.K, seed=self.seed)
@@ -431,11 +434,17 @@ class LaneSweep(Workload):
 
 class EmbedRows(Workload):
     """Scaled embedding rows: 4096 token ids gathered from the tied head's table
-    (262144 x 5376, 4-bit g64) times bf16(sqrt(5376)).  Bytes = the gathered
-    rows' packed bytes + the ids + the bf16 output."""
+    (262144 x 5376, 4-bit g64) times bf16(sqrt(5376)), read from the table's
+    row-contiguous copy (affqmm_embed_rows_copy; the copy is made once, before
+    timing, like the packing).  Bytes = the gathered rows' packed bytes + the
+    ids + the bf16 output.  Steps rotate over 16 id sets and 4 output buffers
+    so that neither the rows nor the output stay in L2 between steps."""
     name = "embed_rows"
     default_steps = 500
     T = 4096
+    ID_SETS = 16
+    OUT_SETS = 4
+    from_copy = True
 
     def make_cases(self, api, synth, device):
         import torch
@@ -444,13 +453,26 @@ class EmbedRows(Workload):
         codes, s, b = synth.affine_table(4, 64, N, K, g, device)
         self.w = api.pack(codes, s, b, 4, 64)
         del codes, s, b
-        self.ids = torch.randint(0, N, (self.T,), generator=g, device=device, dtype=torch.int32)
-        self.out = torch.empty(self.T, K, dtype=torch.bfloat16, device=device)
+        self.rows = api.pack_rows(self.w) if self.from_copy else None
+        self.ids = [torch.randint(0, N, (self.T,), generator=g, device=device, dtype=torch.int32)
+                    for _ in range(self.ID_SETS)]
+        self.outs = [torch.empty(self.T, K, dtype=torch.bfloat16, device=device) for _ in range(self.OUT_SETS)]
         self.N, self.K = N, K
         return []
 
+    def gather(self, ids, out):
+        if self.from_copy:
+            self.api.embed_rows_copy(self.w, self.rows, ids, math.sqrt(5376.0), out=out)
+        else:
+            self.api.embed_rows(self.w, ids, math.sqrt(5376.0), out=out)
+
     def step(self, i: int):
-        self.api.embed_rows(self.w, self.ids, math.sqrt(5376.0), out=self.out)
+        self.gather(self.ids[i % self.ID_SETS], self.outs[i % self.OUT_SETS])
+
+    def step_e2e(self, i: int):
+        """The end-to-end step: the ids uploaded to and the rows read back from
+        the first buffers."""
+        self.gather(self.ids[0], self.outs[0])
 
     launches_per_step = 1
     kernels_per_step = 1
@@ -464,25 +486,37 @@ class EmbedRows(Workload):
         return float(self.T * (self.packed_row_bytes + 4 + 2 * self.K))
 
     def roofline_info(self):
-        return dict(kernel="embed_kernel<4,64>", bound="hbm", units_per_step=self.units_per_step, unit="GB/s",
+        kernel = f"embed_kernel<4,64,{'true' if self.from_copy else 'false'}>"
+        return dict(kernel=kernel, bound="hbm", units_per_step=self.units_per_step, unit="GB/s",
                     traffic_key=f"embed {self.name}")
 
     def l2_note(self) -> str:
-        return "inputs larger than L2: 4096 random rows of a 1.5 GB packed table, 44 MB written per step"
+        rot = self.ID_SETS * self.T * self.packed_row_bytes + self.OUT_SETS * self.T * self.K * 2
+        return (f"inputs larger than L2: steps rotate over {self.ID_SETS} sets of {self.T} random rows of a 1.5 GB "
+                f"table and {self.OUT_SETS} output buffers ({rot / 1e6:.0f} MB touched per rotation > 129 MB L2)")
 
     def describe(self):
-        return f"{self.name}: T={self.T} ids into {self.N}x{self.K} 4-bit g64, scale bf16(sqrt(5376))"
+        src = "its row-contiguous copy" if self.from_copy else "the packed blocks"
+        return (f"{self.name}: T={self.T} ids into {self.N}x{self.K} 4-bit g64 (read from {src}), "
+                f"scale bf16(sqrt(5376))")
 
     def config(self):
         return {"workload": self.describe(), "T": self.T, "N": self.N, "K": self.K, "bits": 4, "group": 64,
                 "l2": self.l2_note(), "parallelism": "replicas"}
 
     def e2e_io(self):
-        return [self.ids], [self.out]
+        return [self.ids[0]], [self.outs[0]]
+
+
+class EmbedRowsBlocks(EmbedRows):
+    """The same gather read from the packed blocks (the tied head's own layout, no copy)."""
+    name = "embed_rows_blocks"
+    from_copy = False
 
 
 WORKLOADS = {"gate_up_decode": GateUpDecode, "decode_step": DecodeStep, "prompt_chunk": PromptChunk,
-             "lane_sweep": LaneSweep, "tiny": Tiny, "embed_rows": EmbedRows, "gate_up_exact": GateUpExact}
+             "lane_sweep": LaneSweep, "tiny": Tiny, "embed_rows": EmbedRows, "embed_rows_blocks": EmbedRowsBlocks,
+             "gate_up_exact": GateUpExact}
 
 
 # ----------------------------------------------------------------------------- timing
@@ -607,7 +641,7 @@ def time_e2e(wl, steps: int, device):
             continue
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
-        wl.step(i)
+        getattr(wl, "step_e2e", wl.step)(i)
         for d, h in zip(outs, h_out):
             h.copy_(d, non_blocking=True)
     e1.record(stream)
@@ -699,6 +733,8 @@ WORKLOAD_ORACLE_SHAPES = {   # the projection each workload's oracle sample take
     "lane_sweep": lambda s: dict(bits=4, group=64, M=2, N=s.SWEEP_SHAPE["N"], K=s.SWEEP_SHAPE["K"],
                                  seed=s.SWEEP_SHAPE["seed"]),
     "embed_rows": lambda s: dict(bits=4, group=64, M=1, N=4096, K=s.HEAD_SHAPE[1], seed=s.EMBED_SEED, embed=True),
+    "embed_rows_blocks": lambda s: dict(bits=4, group=64, M=1, N=4096, K=s.HEAD_SHAPE[1], seed=s.EMBED_SEED,
+                                        embed=True),
     "gate_up_exact": lambda s: dict(s.GATE_UP_DECODE, exact=True),
 }
 

@@ -72,6 +72,9 @@ def lib() -> ctypes.CDLL:
             "affqmm_test_fault_wait": (i32, [i64]),
             "affqmm_run_exact_sums": (i32, [wp, vp, vp, i64, vp, vp, ctypes.c_size_t, vp]),
             "affqmm_run_geglu": (i32, [wp, vp, vp, i64, i32, vp, vp, ctypes.c_size_t, vp]),
+            "affqmm_rows_bytes": (i32, [i32, i32, i64, i64, szp]),
+            "affqmm_pack_rows": (i32, [wp, vp, vp]),
+            "affqmm_embed_rows_copy": (i32, [wp, vp, vp, i64, i32, ctypes.c_uint16, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -372,10 +375,7 @@ def run_noalloc(w: PackedWeight, x: torch.Tensor, y: torch.Tensor, stream=None) 
     return y
 
 
-def embed_rows(w: PackedWeight, ids: torch.Tensor, scale: float | None = None, out: torch.Tensor | None = None,
-               status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """out[t, k] = bf16(W[ids[t], k] * bf16(scale)) (or W's rows when scale is None),
-    W = bf16(s*q + b): rows gathered from the packed table.  ids: int32 CUDA [T]."""
+def _embed_args(w: PackedWeight, ids: torch.Tensor, scale, out):
     if not ids.is_cuda or ids.dtype != torch.int32 or ids.dim() != 1 or not ids.is_contiguous():
         raise ValueError("ids must be a contiguous int32 CUDA vector")
     T = ids.shape[0]
@@ -384,8 +384,45 @@ def embed_rows(w: PackedWeight, ids: torch.Tensor, scale: float | None = None, o
     if out.dtype != torch.bfloat16 or tuple(out.shape) != (T, w.K) or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous bf16 [{T}, {w.K}] tensor")
     sbits = 0 if scale is None else int(torch.tensor([scale], dtype=torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+    return T, out, sbits
+
+
+def embed_rows(w: PackedWeight, ids: torch.Tensor, scale: float | None = None, out: torch.Tensor | None = None,
+               status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[t, k] = bf16(W[ids[t], k] * bf16(scale)) (or W's rows when scale is None),
+    W = bf16(s*q + b): rows gathered from the packed table.  ids: int32 CUDA [T]."""
+    T, out, sbits = _embed_args(w, ids, scale, out)
     cw = w.cstruct()
     _check(lib().affqmm_embed_rows(ctypes.byref(cw), ids.data_ptr(), T, 0 if scale is None else 1, sbits,
                                    out.data_ptr(), status.data_ptr() if status is not None else None,
                                    _stream_ptr(stream)), "affqmm_embed_rows")
+    return out
+
+
+def rows_bytes(bits: int, group: int, N: int, K: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().affqmm_rows_bytes(bits, group, N, K, ctypes.byref(out)), "affqmm_rows_bytes")
+    return out.value
+
+
+def pack_rows(w: PackedWeight, stream=None) -> torch.Tensor:
+    """The row-contiguous copy of a packed table that embed_rows_copy gathers from."""
+    nbytes = rows_bytes(w.bits, w.group, w.N, w.K)
+    rows = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=w.packed.device)
+    cw = w.cstruct()
+    _check(lib().affqmm_pack_rows(ctypes.byref(cw), rows.data_ptr(), _stream_ptr(stream)), "affqmm_pack_rows")
+    return rows
+
+
+def embed_rows_copy(w: PackedWeight, rows: torch.Tensor, ids: torch.Tensor, scale: float | None = None,
+                    out: torch.Tensor | None = None, status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """embed_rows, reading the rows from `rows` = pack_rows(w) (the same values)."""
+    T, out, sbits = _embed_args(w, ids, scale, out)
+    if not rows.is_cuda or rows.dtype != torch.uint8 or rows.numel() < rows_bytes(w.bits, w.group, w.N, w.K):
+        raise ValueError("rows must be the uint8 CUDA copy made by pack_rows(w)")
+    cw = w.cstruct()
+    _check(lib().affqmm_embed_rows_copy(ctypes.byref(cw), rows.data_ptr(), ids.data_ptr(), T,
+                                        0 if scale is None else 1, sbits, out.data_ptr(),
+                                        status.data_ptr() if status is not None else None, _stream_ptr(stream)),
+           "affqmm_embed_rows_copy")
     return out

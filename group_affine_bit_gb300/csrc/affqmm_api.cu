@@ -236,7 +236,7 @@ int plan_prompt(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, Pr
         ctas += P.nctas;
         tiles_total += tiles;
     }
-    if (4 * tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
+    if (tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
     plan->grid = (int)ctas;
     plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kPromptSlotFloats * sizeof(float) : 0;
     return AFFQMM_OK;
@@ -366,6 +366,28 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         if (rc) return rc;
         if (launch_prompt(ws[0].bits, plan.p, map, plan.grid, st) != cudaSuccess) return AFFQMM_E_CUDA;
     }
+    return AFFQMM_OK;
+}
+
+// The gather from either form of the table: `rows` NULL reads the packed
+// blocks of w, else the row-contiguous copy that affqmm_pack_rows made of w.
+int embed_impl(const affqmm_weight* w, const void* rows, bool rowcopy, const int32_t* ids, int64_t T, int has_scale,
+               uint16_t scale, uint16_t* out, uint32_t* status, void* stream) {
+    int rc = check_weight(w);
+    if (rc) return rc;
+    if (T < 0) return AFFQMM_E_ARG;
+    if (T == 0 || w->K == 0) return AFFQMM_OK;
+    if (!ids || !out || (rowcopy && !rows)) return AFFQMM_E_NULL;
+    if (w->N == 0) return AFFQMM_E_SHAPE;  // no row to gather
+    if (!aligned(out, 16) || !aligned(ids, 4) || (status && !aligned(status, 4)) || (rowcopy && !aligned(rows, 256)))
+        return AFFQMM_E_ALIGN;
+    if (T > ((int64_t)1 << 31) / ((w->K + KBLK - 1) / KBLK)) return AFFQMM_E_SHAPE;
+    DeviceInfo* d = nullptr;
+    rc = device_info(&d);
+    if (rc) return rc;
+    if (launch_embed(w->bits, w->group, rowcopy, rowcopy ? rows : w->packed, w->N, w->K, ids, T, has_scale ? 1 : 0,
+                     scale, out, status, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return AFFQMM_E_CUDA;
     return AFFQMM_OK;
 }
 
@@ -516,21 +538,33 @@ int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* stream) {
 
 int affqmm_embed_rows(const affqmm_weight* w, const int32_t* ids, int64_t T, int has_scale, uint16_t scale,
                       uint16_t* out, uint32_t* status, void* stream) {
-    int rc = check_weight(w);
+    return embed_impl(w, nullptr, false, ids, T, has_scale, scale, out, status, stream);
+}
+
+int affqmm_rows_bytes(int bits, int group, int64_t N, int64_t K, size_t* bytes) {
+    size_t packed = 0;
+    const int rc = affqmm_packed_bytes(bits, group, N, K, &packed);  // the same argument checks
     if (rc) return rc;
-    if (T < 0) return AFFQMM_E_ARG;
-    if (T == 0 || w->K == 0) return AFFQMM_OK;
-    if (!ids || !out) return AFFQMM_E_NULL;
-    if (w->N == 0) return AFFQMM_E_SHAPE;  // no row to gather
-    if (!aligned(out, 16) || !aligned(ids, 4) || (status && !aligned(status, 4))) return AFFQMM_E_ALIGN;
-    if (T > ((int64_t)1 << 31) / ((w->K + KBLK - 1) / KBLK)) return AFFQMM_E_SHAPE;
-    DeviceInfo* d = nullptr;
-    rc = device_info(&d);
+    const int KB = (int)((K + KBLK - 1) / KBLK);
+    *bytes = (size_t)N * (size_t)rows_stride(bits, group, KB);
+    return AFFQMM_OK;
+}
+
+int affqmm_pack_rows(const affqmm_weight* w, void* rows, void* stream) {
+    const int rc = check_weight(w);
     if (rc) return rc;
-    if (launch_embed(w->bits, w->group, w->packed, w->N, w->K, ids, T, has_scale ? 1 : 0, scale, out, status,
-                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (w->N == 0 || w->K == 0) return AFFQMM_OK;
+    if (!rows) return AFFQMM_E_NULL;
+    if (!aligned(rows, 256)) return AFFQMM_E_ALIGN;
+    if (launch_pack_rows(w->bits, w->group, w->packed, w->N, w->K, rows, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
         return AFFQMM_E_CUDA;
     return AFFQMM_OK;
+}
+
+int affqmm_embed_rows_copy(const affqmm_weight* w, const void* rows, const int32_t* ids, int64_t T, int has_scale,
+                           uint16_t scale, uint16_t* out, uint32_t* status, void* stream) {
+    return embed_impl(w, rows, true, ids, T, has_scale, scale, out, status, stream);
 }
 
 int affqmm_workspace_status(void* workspace, void* stream) {

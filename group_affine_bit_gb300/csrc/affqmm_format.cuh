@@ -62,6 +62,21 @@ __host__ __device__ constexpr int sb_offset(int bits, int group, int n) {
     return code_bytes(bits) + n * 4 * sb_words(group);
 }
 
+// The row-contiguous copy of a packed table that the embedding gather reads
+// (affqmm_pack_rows): the same words as the blocks above, regrouped by row so
+// that one row's bytes are one contiguous range.  Row n starts at
+// n * rows_stride; in it come the 4*bits code words of each 128-deep block
+// in block order (the words load_row_codes returns, in that order), then the
+// scale/bias words of every block in block order; the stride is padded to
+// 16 bytes.
+__host__ __device__ constexpr int64_t rows_stride(int bits, int group, int KB) {
+    return ((int64_t)KB * (16 * bits + 4 * sb_words(group)) + 15) / 16 * 16;
+}
+__host__ __device__ constexpr int64_t rows_codes_offset(int bits, int kb) { return (int64_t)kb * 16 * bits; }
+__host__ __device__ constexpr int64_t rows_sb_offset(int bits, int group, int KB, int kb) {
+    return (int64_t)KB * 16 * bits + (int64_t)kb * 4 * sb_words(group);
+}
+
 #if defined(__CUDACC__)
 
 // ---------------------------------------------------------------- bf16x2 ops
@@ -176,6 +191,13 @@ __device__ __forceinline__ void load_row_codes(const uint8_t* blk, int n, uint32
         uint32_t* d = cw + 4 * P0;
         ld_stream_v4(q, d[4 * c], d[4 * c + 1], d[4 * c + 2], d[4 * c + 3]);
     }
+}
+
+// The same words from a row of the row-contiguous copy (16-byte aligned).
+template <int BITS>
+__device__ __forceinline__ void load_rowcopy_codes(const uint8_t* p, uint32_t* cw) {
+#pragma unroll
+    for (int v = 0; v < BITS; ++v) ld_stream_v4(p + 16 * v, cw[4 * v], cw[4 * v + 1], cw[4 * v + 2], cw[4 * v + 3]);
 }
 
 // The same words from a block staged in shared memory (same layout).

@@ -69,7 +69,7 @@ struct PromptProj {
     int32_t units;        // tiles * k-blocks
     int32_t nctas;        // CTAs working on this projection (<= units)
     int32_t cta_begin;    // first CTA of this projection in the grid
-    int32_t ctr_begin;    // first tile of this projection's merge counters (four per tile)
+    int32_t ctr_begin;    // first tile of this projection's merge counters (one per 256-row tile)
     int32_t slot_begin;   // first partial slot (two per CTA)
 };
 
@@ -125,8 +125,13 @@ cudaError_t launch_pack(int bits, int group, int64_t N, int64_t K, const uint8_t
                         cudaStream_t st);
 cudaError_t launch_dequant(int bits, int group, int64_t N, int64_t K, const void* packed,
                            uint16_t* out, cudaStream_t st);
-// embed.cu: rows ids[0..T) of the table, optionally times a bf16 scale.
-cudaError_t launch_embed(int bits, int group, const void* packed, int64_t N, int64_t K, const int32_t* ids,
-                         int64_t T, int has_scale, uint16_t scale, uint16_t* out, uint32_t* status, cudaStream_t st);
+// embed.cu: rows ids[0..T) of the table (the packed blocks, or their
+// row-contiguous copy when `rowcopy`), optionally times a bf16 scale; and the
+// row-contiguous copy of a packed table.
+cudaError_t launch_embed(int bits, int group, bool rowcopy, const void* table, int64_t N, int64_t K,
+                         const int32_t* ids, int64_t T, int has_scale, uint16_t scale, uint16_t* out, uint32_t* status,
+                         cudaStream_t st);
+cudaError_t launch_pack_rows(int bits, int group, const void* packed, int64_t N, int64_t K, void* rows,
+                             cudaStream_t st);
 
 }  // namespace affqmm

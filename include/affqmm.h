@@ -278,6 +278,31 @@ AFFQMM_API int affqmm_dequant(const affqmm_weight* w, uint16_t* w_out, void* str
 AFFQMM_API int affqmm_embed_rows(const affqmm_weight* w, const int32_t* ids, int64_t T, int has_scale,
                                  uint16_t scale, uint16_t* out, uint32_t* status, void* stream);
 
+/* The embedding gather from a row-contiguous copy of the table (an
+ * extension with no counterpart on the pages; the values are those of
+ * affqmm_embed_rows, bit for bit).  The packed blocks keep a row's bytes
+ * between those of 31 other rows, so a gather of scattered rows from them
+ * fetches several times the bytes it uses; the copy keeps each row's bytes
+ * in one contiguous range.  It is made once per table, on the device, by
+ * affqmm_pack_rows, and costs about as much memory as the packed table.
+ *
+ * affqmm_rows_bytes: bytes of the copy of an N x K table (host call):
+ *   N * stride, stride = ceil(K/128) * (16*bits + 512/group) bytes rounded
+ *   up to 16.  Errors as affqmm_packed_bytes.
+ * affqmm_pack_rows: write the copy of the packed weight w into `rows`
+ *   (device, affqmm_rows_bytes() bytes, 256-byte aligned).  Like
+ *   affqmm_pack, the kernel makes its writes visible device-wide before it
+ *   finishes.  Errors: E_NULL, E_BITS, E_GROUP, E_SHAPE, E_ALIGN, E_CUDA.
+ * affqmm_embed_rows_copy: affqmm_embed_rows with the rows read from `rows`,
+ *   a copy that affqmm_pack_rows made of w (w itself is only read for its
+ *   bits, group, N and K; its packed pointer must still be valid).  Same
+ *   arguments, results and errors, plus E_NULL / E_ALIGN for `rows`. */
+AFFQMM_API int affqmm_rows_bytes(int bits, int group, int64_t N, int64_t K, size_t* bytes);
+AFFQMM_API int affqmm_pack_rows(const affqmm_weight* w, void* rows, void* stream);
+AFFQMM_API int affqmm_embed_rows_copy(const affqmm_weight* w, const void* rows, const int32_t* ids, int64_t T,
+                                      int has_scale, uint16_t scale, uint16_t* out, uint32_t* status,
+                                      void* stream);
+
 /* Read the device status word of a workspace that run calls used
  * (synchronizes `stream`).  Returns AFFQMM_OK, or AFFQMM_E_TIMEOUT when a
  * kernel that used this workspace gave up a bounded wait (its outputs are

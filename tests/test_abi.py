@@ -26,7 +26,8 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for want in ["affqmm_pack", "affqmm_run", "affqmm_run_stacked", "affqmm_dequant",
-                 "affqmm_packed_bytes", "affqmm_workspace_bytes", "affqmm_strerror"]:
+                 "affqmm_packed_bytes", "affqmm_workspace_bytes", "affqmm_strerror",
+                 "affqmm_embed_rows", "affqmm_rows_bytes", "affqmm_pack_rows", "affqmm_embed_rows_copy"]:
         assert want in names
 
 
@@ -57,6 +58,20 @@ def test_packed_bytes_closed_form(bits, group):
         kb = -(-K // 128)             # 128-deep blocks
         want = tiles * kb * (128 * 128 * bits // 8 + 128 * 4 * (128 // group))
         assert api.packed_bytes(bits, group, N, K) == want
+
+
+@pytest.mark.parametrize("bits,group", [(b, g) for b in (2, 3, 4, 5, 6, 8) for g in (32, 64, 128)])
+def test_rows_bytes_closed_form(bits, group):
+    """The row-contiguous copy: N rows of ceil(K/128) blocks x (16*bits code
+    bytes + 512/group scale/bias bytes), the row padded to 16 bytes."""
+    for N, K in [(512, 256), (262144, 5376), (17, 96 if group == 32 else 2 * group), (1, group), (0, 0)]:
+        if K % group:
+            continue
+        kb = -(-K // 128)
+        stride = -(-(kb * (16 * bits + 512 // group)) // 16) * 16
+        assert api.rows_bytes(bits, group, N, K) == N * stride
+    with pytest.raises(api.AffqmmError):
+        api.rows_bytes(bits, group, 16, group + 16)
 
 
 @pytest.mark.parametrize("bits,group,N,K,status", [
@@ -165,6 +180,22 @@ def test_embed_rows_refusals_before_any_launch(L):
     assert api.STATUS_NAMES[rc] == "AFFQMM_E_NULL"
     rc = L.affqmm_embed_rows(ctypes.byref(w), 0x200000, 4, 1, 0x4000, 0x300008, None, None)
     assert api.STATUS_NAMES[rc] == "AFFQMM_E_ALIGN"
+
+
+def test_row_copy_refusals_before_any_launch(L):
+    names = api.STATUS_NAMES
+    w = _w()
+    assert names[L.affqmm_pack_rows(ctypes.byref(w), None, None)] == "AFFQMM_E_NULL"
+    assert names[L.affqmm_pack_rows(ctypes.byref(w), 0x400010, None)] == "AFFQMM_E_ALIGN"
+    assert names[L.affqmm_pack_rows(ctypes.byref(_w(bits=7)), 0x400000, None)] == "AFFQMM_E_BITS"
+    assert L.affqmm_pack_rows(ctypes.byref(_w(N=0)), None, None) == 0     # nothing to copy
+    copy = lambda rows, ids=0x200000, out=0x300000, T=4: L.affqmm_embed_rows_copy(
+        ctypes.byref(w), rows, ids, T, 1, 0x4000, out, None, None)
+    assert names[copy(None)] == "AFFQMM_E_NULL"
+    assert names[copy(0x400010)] == "AFFQMM_E_ALIGN"
+    assert names[copy(0x400000, T=-1)] == "AFFQMM_E_ARG"
+    assert names[copy(0x400000, out=0x300008)] == "AFFQMM_E_ALIGN"
+    assert copy(None, T=0) == 0
 
 
 def test_fault_wait_hook_refusal_and_reset(L):
