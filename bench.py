@@ -249,9 +249,8 @@ class Case:
 
     @property
     def kernels(self) -> int:
-        """All of the library's kernel launches (one per 128-row chunk; the
-        split-depth merge runs inside the projection kernel)."""
-        return self.launches
+        """All of the library's kernel launches: a prompt chunk also launches its merge kernel."""
+        return 1 if self.M <= 16 else 2 * (-(-self.M // 128))
 
     def oracle_shape(self):
         return dict(bits=self.bits, group=self.group, M=self.M, N=self.N, K=self.K, seed=self.seed)

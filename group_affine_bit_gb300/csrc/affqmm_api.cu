@@ -236,7 +236,7 @@ int plan_prompt(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, Pr
         ctas += P.nctas;
         tiles_total += tiles;
     }
-    if (tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
+    if (tiles_total > 65535) return AFFQMM_E_SHAPE;  // one merge-kernel grid row per 256-row tile
     plan->grid = (int)ctas;
     plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kPromptSlotFloats * sizeof(float) : 0;
     return AFFQMM_OK;

@@ -69,7 +69,7 @@ struct PromptProj {
     int32_t units;        // tiles * k-blocks
     int32_t nctas;        // CTAs working on this projection (<= units)
     int32_t cta_begin;    // first CTA of this projection in the grid
-    int32_t ctr_begin;    // first tile of this projection's merge counters (one per 256-row tile)
+    int32_t ctr_begin;    // first 256-row tile of this projection in the merge kernel's grid
     int32_t slot_begin;   // first partial slot (two per CTA)
 };
 

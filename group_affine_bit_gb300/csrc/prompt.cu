@@ -23,12 +23,8 @@
 //     (one issuing thread cannot keep the tensor pipe busy at these sizes);
 //   * at the end of a tile's segment four epilogue warps read the two
 //     accumulators with tcgen05.ld and store bf16 y, or, when several runs
-//     share the tile, an fp32 partial;
-//   * after its last segment the whole CTA meets the other runs of each tile
-//     it shares (a counter per tile, a bounded wait until every run has
-//     stored its partial) and adds the runs' partials in run (k) order for
-//     its own slab of the tile's rows, so that every run of a shared tile
-//     takes a part of the merge and no second kernel is needed.
+//     share the tile, an fp32 partial; a second, small kernel then adds each
+//     shared tile's partials in run (k) order, every output in parallel.
 // Prior art: the affine_mm prompt GEMM of the "Gemma 4 12B on the native
 // Metal engine" page, which dequantizes each weight as bf16(fma(scale, code,
 // bias)) into the tile and lets the tensor unit accumulate over the whole
@@ -105,109 +101,6 @@ constexpr int prm_wring() {
 template <int BITS, int GROUP>
 constexpr size_t prm_ring_bytes() {
     return (size_t)prm_xring<BITS, GROUP>() * P_X_BYTES + (size_t)prm_wring<BITS, GROUP>() * prm_wstage<BITS, GROUP>();
-}
-
-// The partial of run `cb` for the tile that starts at unit t0: the run's
-// first slot when its run begins inside the tile, else its second (the tile
-// is then the last segment of a run that began in an earlier tile).
-__device__ __forceinline__ const float* run_partial(const PromptParams& p, const PromptProj& P, int cb, int t0,
-                                                    int U, int PC) {
-    const int b0 = (int)((int64_t)cb * U / PC);
-    return p.slots + (size_t)(P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1)) * kPromptSlotFloats;
-}
-
-// The tiles that several runs share, merged inside the kernel.  A CTA's run
-// has at most two such tiles (its first and its last segment); the CTA adds
-// one to each tile's counter once its partials are stored, then, per tile,
-// waits until all nr runs have, and writes y for its slab of the tile's 256
-// rows (run r of the tile takes rows [256 r / nr, 256 (r+1) / nr), in
-// multiples of four) as the runs' partials added in run order -- the same
-// sum, in the same order, for every output whichever run writes it.  A
-// second arrival after the slab lets the last run of the tile reset the
-// counter to zero for the next call.  Every thread of the CTA takes part:
-// a thread owns four consecutive rows n of one activation row m (a 16-byte
-// load from each run's partial) and keeps four runs' loads in flight.
-__device__ void merge_shared_tiles(const PromptParams& p, const PromptProj& P, int c, int u0, int u1, int M,
-                                   volatile int* abort_flag) {
-    const int U = P.units, PC = P.nctas, KB = p.KB;
-    const int tf = u0 / KB, tl = (u1 - 1) / KB;
-    const bool share_f = run_of(tf * KB, U, PC) != run_of(tf * KB + KB - 1, U, PC);
-    const bool share_l = tl != tf && run_of(tl * KB, U, PC) != run_of(tl * KB + KB - 1, U, PC);
-    if (!share_f && !share_l) return;
-    __shared__ int go;
-    // every thread's partial stores (the epilogue warps') are ordered before
-    // the arrivals below
-    fence_acq_rel_gpu();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (share_f) atom_add_acq_rel(p.counters + P.ctr_begin + tf, 1u);
-        if (share_l) atom_add_acq_rel(p.counters + P.ctr_begin + tl, 1u);
-    }
-#pragma unroll 1
-    for (int i = 0; i < 2; ++i) {
-        if (!(i == 0 ? share_f : share_l)) continue;
-        const int tile = i == 0 ? tf : tl;
-        const int t0 = tile * KB;
-        const int cf = run_of(t0, U, PC), cl = run_of(t0 + KB - 1, U, PC);
-        const int nr = cl - cf + 1, r = c - cf;
-        unsigned* ctr = p.counters + P.ctr_begin + tile;
-        if (threadIdx.x == 0) {
-            bool ok = true;
-            if (ld_acquire_gpu(ctr) < (unsigned)nr) {
-                const long long w0 = clock64();
-                while (ld_acquire_gpu(ctr) < (unsigned)nr) {
-                    if (*abort_flag || clock64() - w0 > kWaitLimitCycles) {
-                        ok = false;
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-            }
-            if (!ok && !*abort_flag) {
-                *abort_flag = 1;
-                atomicOr(p.status, 1u);
-            }
-            go = ok;
-        }
-        __syncthreads();
-        if (!go) return;
-        fence_acq_rel_gpu();  // the other runs' partials are read after the counter
-        const int r0 = 4 * (64 * r / nr), r1 = 4 * (64 * (r + 1) / nr);
-        const int wq = (r1 - r0) / 4;  // 16-byte columns of the slab
-        const int items = M * wq;
-        const float* first = run_partial(p, P, cf, t0, U, PC);
-        for (int it = (int)threadIdx.x; it < items; it += P_THREADS) {
-            const int m = it / wq;
-            const int n4 = r0 + 4 * (it - m * wq);
-            const int64_t n = (int64_t)tile * P_TILE_N + n4;
-            if (n >= P.N) continue;
-            const size_t off = (size_t)m * P_TILE_N + n4;
-            float4 acc = __ldcg(reinterpret_cast<const float4*>(first + off));
-#pragma unroll 1
-            for (int cb = cf + 1; cb <= cl; cb += 4) {
-                float4 f[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (cb + j <= cl) f[j] = __ldcg(reinterpret_cast<const float4*>(run_partial(p, P, cb + j, t0, U, PC) + off));
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (cb + j <= cl) {
-                        acc.x += f[j].x;
-                        acc.y += f[j].y;
-                        acc.z += f[j].z;
-                        acc.w += f[j].w;
-                    }
-            }
-            uint16_t* yr = P.y + (int64_t)m * P.N + n;
-            const float av[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (n + e < P.N) yr[e] = __bfloat16_as_ushort(__float2bfloat16_rn(av[e]));
-        }
-        __syncthreads();
-        // the slab is written; the last of the tile's 2 nr arrivals zeroes the counter
-        if (threadIdx.x == 0 && atom_add_acq_rel(ctr, 1u) == (unsigned)(2 * nr - 1)) atomicExch(ctr, 0u);
-    }
 }
 
 template <int BITS, int GROUP>
@@ -430,7 +323,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 }
             }
             // accumulators drained: the MMA thread may start the next segment
-            // (a partial is added to the other runs' by merge_shared_tiles)
+            // (a partial is added to the other runs' by prompt_merge_kernel)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(acc_empty, 0));
@@ -448,7 +341,49 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, P_TMEM_COLS);
     }
-    if (u0 < u1 && !*abort_flag) merge_shared_tiles(p, P, c, u0, u1, p.M, abort_flag);
+}
+
+// The tiles that several runs share: y = the runs' fp32 partials added in run
+// order.  Grid: (4-row blocks of the activation rows, every tile of every
+// projection); a thread owns four consecutive weight rows n of one activation
+// row m (a 16-byte load from each run's partial: a warp reads 512 contiguous
+// bytes), so the whole merge is a few rounds of fully parallel L2 reads.
+// Tiles that one run owned were stored by prompt_kernel and are skipped.
+constexpr int P_MERGE_THREADS = 256;
+__global__ void __launch_bounds__(P_MERGE_THREADS) prompt_merge_kernel(const __grid_constant__ PromptParams p) {
+    pdl_launch_dependents();  // the next kernel's prologue and weight copies may start
+    pdl_wait();               // the partials of prompt_kernel are complete and visible
+    const int t_all = (int)blockIdx.y;
+    int pi = 0;
+    for (int i = 1; i < p.nproj; ++i)
+        if (t_all >= p.proj[i].ctr_begin) pi = i;
+    const PromptProj& P = p.proj[pi];
+    const int tile = t_all - P.ctr_begin;
+    const int U = P.units, PC = P.nctas, KB = p.KB;
+    const int t0 = tile * KB, t1 = t0 + KB - 1;
+    const int cf = run_of(t0, U, PC), cl = run_of(t1, U, PC);
+    if (cf == cl) return;
+    const int m = 4 * (int)blockIdx.x + ((int)threadIdx.x >> 6);
+    const int n4 = 4 * ((int)threadIdx.x & 63);  // weight row within the 256-row tile
+    const int64_t n = (int64_t)tile * P_TILE_N + n4;
+    if (m >= p.M || n >= P.N) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int cb = cf; cb <= cl; ++cb) {
+        const int b0 = (int)((int64_t)cb * U / PC);
+        const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
+        const float4 f = __ldcg(
+            reinterpret_cast<const float4*>(p.slots + (size_t)sc * kPromptSlotFloats + (size_t)m * P_TILE_N + n4));
+        acc.x += f.x;
+        acc.y += f.y;
+        acc.z += f.z;
+        acc.w += f.w;
+    }
+    uint16_t* yr = P.y + (int64_t)m * P.N + n;
+    const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        if (n + e < P.N) yr[e] = __bfloat16_as_ushort(__float2bfloat16_rn(av[e]));
 }
 
 template <int BITS, int GROUP>
@@ -458,7 +393,11 @@ size_t prompt_smem_for() {
 
 template <int BITS, int GROUP>
 cudaError_t launch_prompt_bg(const PromptParams& p, const CUtensorMap& map, int grid, cudaStream_t st) {
-    return launch_pdl(prompt_kernel<BITS, GROUP>, grid, P_THREADS, prompt_smem_for<BITS, GROUP>(), st, p, map);
+    cudaError_t e = launch_pdl(prompt_kernel<BITS, GROUP>, grid, P_THREADS, prompt_smem_for<BITS, GROUP>(), st, p, map);
+    if (e != cudaSuccess) return e;
+    const PromptProj& last = p.proj[p.nproj - 1];
+    const dim3 mgrid((unsigned)((p.M + 3) / 4), (unsigned)(last.ctr_begin + last.tiles));
+    return launch_pdl(prompt_merge_kernel, mgrid, P_MERGE_THREADS, 0, st, p);
 }
 
 template <int BITS>
