@@ -76,9 +76,35 @@ __global__ void __launch_bounds__(E_THREADS) embed_kernel(const uint8_t* __restr
             for (int c = 0; c < KBLK / 2; ++c) w[c] = bf2_mul(w[c], scale2);
         }
     }
+    // When the depth is whole blocks, item i's values are out[128 i ..
+    // 128 i + 127], so a warp's 32 items are one contiguous 8 KB range: the
+    // warp stages its items in shared memory and writes the range as 16
+    // stores of 512 contiguous bytes.  (A thread's own 16 stores would put
+    // 16 bytes in each of 32 lines per instruction.)  The 16-byte slot of
+    // piece c of lane L is L*16 + (c ^ (L & 7)), so that the eight lanes of
+    // one store phase, either way round, touch eight different bank groups.
+    __shared__ uint4 stage[E_THREADS / 32][32 * 16];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int64_t item0 = item - lane;
+    if (KB * (int64_t)KBLK == K && item0 + 31 < T * KB) {
+        uint4* st = stage[wid];
 #pragma unroll
-    for (int c = 0; c < KBLK / 8; ++c)  // 8 values (16 bytes) per store
-        if (8 * c < kleft) st_v4(dst + 8 * c, w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        for (int c = 0; c < KBLK / 8; ++c)
+            st[lane * 16 + (c ^ (lane & 7))] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        __syncwarp();
+        uint16_t* base = out + item0 * KBLK;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int u = 32 * i + lane;  // 16-byte piece of the warp's range
+            const int owner = u >> 4, c = u & 15;
+            const uint4 v = st[owner * 16 + (c ^ (owner & 7))];
+            st_v4(base + 8 * u, v.x, v.y, v.z, v.w);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < KBLK / 8; ++c)  // 8 values (16 bytes) per store
+            if (8 * c < kleft) st_v4(dst + 8 * c, w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
 }
 
 // The row-contiguous copy: one thread per (row n, 128-deep block) moves the
