@@ -19,11 +19,13 @@ over one batch of synthetic input with the weights resident in HBM:
 the decode workloads and TFLOP/s for the prompt chunk.  Weight copies rotate
 so that the bytes touched between two reads of one copy exceed the 129 MB L2.
 Steps are replayed from CUDA graphs and timed with CUDA events on the stream
-that launches them.  `e2e` times the same steps end to end through the C
-ABI's host-buffer call (affqmm_run_host: x uploaded from pinned host memory,
-the projection, y read back, one call per projection); the exact-codes form
-and the embedding gather use the Python API with torch's copies.  `--impl reference` times the CPU
-oracle on a bounded sample of the same workload on the host cores.  Under torchrun every rank runs an
+that launches them.  `e2e` times the same steps end to end with host
+buffers: a one-projection step is one call of the C ABI's host-buffer entry
+point (affqmm_run_host: x uploaded from pinned host memory, the projection,
+y read back); a step of several projections, the exact-codes form and the
+embedding gather upload the step's inputs, run it through the Python API
+and read its outputs back.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload on the host cores.  Under torchrun every rank runs an
 independent replica (the path needs no exchange) and rank 0 reports the
 aggregate over ranks with the slowest rank's time.
 """
@@ -608,11 +610,16 @@ class HostCalls:
 
 
 def time_e2e(wl, steps: int, device):
-    """Same steps end to end with host buffers: activations uploaded from
-    pinned host memory and outputs read back to pinned host memory every step,
-    inside the timed region.  Projections go through the C ABI's host-buffer
-    call (affqmm_run_host); the exact-codes form and the embedding gather,
-    which have none, go through the Python API with torch's copies around it."""
+    """Same steps end to end with host buffers: the step's activations uploaded
+    from pinned host memory at its start and its outputs read back to pinned
+    host memory at its end, inside the timed region.  A step of one projection
+    is one call of the C ABI's host-buffer entry point (affqmm_run_host: upload,
+    projection, read-back).  A step of several projections uploads all of its
+    inputs, runs its projections through the Python API (affqmm_run) and reads
+    all of its outputs back: one host call per projection would put two copies
+    between every pair of launches (about 14 us more per projection on the
+    GPU).  The exact-codes form and the embedding gather, which have no
+    host-buffer call, take the second form too."""
     import torch
     ins, outs = wl.e2e_io()
     h_in = [t.detach().cpu().pin_memory() for t in ins]
@@ -622,7 +629,7 @@ def time_e2e(wl, steps: int, device):
     stream = torch.cuda.current_stream(device)
     cases = getattr(wl, "cases", [])
     host = None
-    if cases and not any(getattr(c, "exact", False) for c in cases):
+    if len(cases) == 1 and not getattr(cases[0], "exact", False):
         host = HostCalls(wl, h_in, h_out, int(stream.cuda_stream))
     for i in range(3):
         if host is not None:
@@ -646,7 +653,8 @@ def time_e2e(wl, steps: int, device):
     e1.record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t0
-    via = "affqmm_run_host (C ABI, host buffers)" if host is not None else "Python API + torch copies"
+    via = ("affqmm_run_host (C ABI, host buffers)" if host is not None
+           else "step inputs uploaded, Python API (affqmm_run), step outputs read back (torch copies)")
     return max(wall, e0.elapsed_time(e1) * 1e-3), bi, bo, via
 
 
