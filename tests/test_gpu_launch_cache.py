@@ -1,0 +1,65 @@
+"""The per-thread cache of launch set-ups (plan + x tensor map) in the C ABI:
+a call whose arguments differ from a cached one in any single value --
+weight, x, y, workspace, M, form -- must not reuse that set-up.  Calls cycle
+through more argument sets than the cache holds, and every output must
+equal the one the same call produced the first time (the library is
+deterministic) and be written where that call asked."""
+import pytest
+import torch
+
+from group_affine_bit_gb300 import api, build, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return api.lib()
+
+
+def bits16(t):
+    return t.view(torch.int16).clone()
+
+
+@pytest.mark.parametrize("M", [1, 16, 100])
+def test_cached_setups_follow_every_argument(M):
+    bits, group, N, K = 4, 64, 384, 1024
+    weights, xs = [], []
+    for i in range(3):
+        x, codes, s, b = synth.problem(bits, group, M, N, K, seed=1200 + 10 * M + i)
+        weights.append(api.pack(codes.cuda(), s.cuda(), b.cuda(), bits, group))
+        xs.append(x.cuda())
+    wss = [api.Workspace(), api.Workspace()]
+    combos = [(wi, xi, wsi) for wi in range(3) for xi in range(3) for wsi in range(2)]
+    first = {}
+    for rnd in range(2):
+        for (wi, xi, wsi) in combos:
+            y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            api.run(weights[wi], xs[xi], y=y, workspace=wss[wsi])
+            torch.cuda.synchronize()
+            assert not torch.isnan(y.float()).any(), f"output not written for {(wi, xi, wsi)}"
+            key = (wi, xi)
+            if key in first:
+                assert torch.equal(bits16(y), first[key]), f"round {rnd}: {(wi, xi, wsi)} differs"
+            else:
+                first[key] = bits16(y)
+    # distinct weights and inputs give distinct outputs (the cache never served another call's set-up)
+    assert not torch.equal(first[(0, 0)], first[(1, 0)]) and not torch.equal(first[(0, 0)], first[(0, 1)])
+
+
+def test_cached_setup_respects_form_and_rows():
+    bits, group, N, K = 4, 64, 256, 512
+    x, codes, s, b = synth.problem(bits, group, 16, N, K, seed=1300)
+    w = api.pack(codes.cuda(), s.cuda(), b.cuda(), bits, group)
+    xd = x.cuda()
+    ws = api.Workspace()
+    ref_rounded = bits16(api.run(w, xd, workspace=ws))
+    ref_exact = bits16(api.run_exact(w, xd, workspace=ws))
+    ref_m5 = bits16(api.run(w, xd[:5].contiguous(), workspace=ws))
+    for _ in range(3):
+        assert torch.equal(bits16(api.run_exact(w, xd, workspace=ws)), ref_exact)
+        assert torch.equal(bits16(api.run(w, xd, workspace=ws)), ref_rounded)
+        assert torch.equal(bits16(api.run(w, xd[:5].contiguous(), workspace=ws)), ref_m5)
