@@ -26,19 +26,26 @@
 //     read, and for each of the 8 16-deep steps rounds four weight pairs --
 //     bf16(fma(s, q, b)), one rounding -- and issues one mma (two when M > 8)
 //     into fp32 registers.
+// At the launch's start a CTA requests two slots' weights and waits for the
+// first to land before it requests the rest of its ring, so that the first
+// slots of all CTAs are not queued behind everyone's later ones.
 // The exact-codes instantiation (the pages' lane projection) puts the exact
 // codes into the A fragments and adds s * sum(q x) + b * sum(x) per group;
-// its activation warp loads the tiles itself and writes each group's sum of
-// x next to them (or copies the sums that the kernel producing x wrote).
+// each group's sum of x comes from one more mma per step with an A fragment
+// of ones, or from the sums that the kernel producing x wrote (copied into
+// the slot with cp.async).
 // The GeGLU form treats the projection as a gate/up stack whose rows are
 // interleaved in 16-row blocks: the two warps of a pair own a gate block and
-// its up block, count in on one counter, and the last to arrive stores
+// its up block; for a whole tile they meet in shared memory, for a cut tile
+// they count in on one counter; the gate warp, or the last to arrive, stores
 // h = gelu_approx(gate) * up as bf16 operations.
 // Work split ("stream-K"): the projection's blocks, numbered tile-major, are
 // cut into one contiguous run per CTA.  A tile cut by run boundaries gets one
 // fp32 partial per run; the last warp to arrive (an atomic counter per tile
 // and 16-row group, no waiting) adds them in run order and resets the
-// counter.  The cut depends only on the projection, M and the device, so the
+// counter.  The run that holds a tile's first blocks reaches them at its
+// end, usually after the other runs have counted in: it then adds their
+// partials to its own registers at once.  The cut depends only on the projection, M and the device, so the
 // same inputs give the same bits on every call, alone or stacked.  Every
 // wait is on an mbarrier with a bound; a wait that gives up sets the
 // workspace status word and an abort flag, and every role finishes.
@@ -64,6 +71,7 @@ constexpr int D_WPROD = D_CWARPS;             // weights producer warp
 constexpr int D_XPROD = D_CWARPS + 1;         // activations producer warp
 constexpr int D_THREADS = (D_CWARPS + 2) * 32;
 constexpr int D_CTAS_PER_SM = 2;
+constexpr int D_FILL_GATE = 2;                // weight slots a CTA requests before its first has landed
 constexpr uint32_t D_XROW = 272;              // bytes per activation row of a tile (128 k + 8 of padding)
 constexpr int D_SLOTS_MAX = 16;
 constexpr uint32_t D_SMEM = 110u * 1024u;     // dynamic shared memory per CTA
@@ -487,6 +495,14 @@ __global__ void __launch_bounds__(D_THREADS, D_CTAS_PER_SM)
             for (int j = 0; j < npairs; ++j) {
                 const int s = j % NS;
                 if (!wait_or_abort_lazy(BAR(empty, s), (uint32_t)((j / NS) & 1) ^ 1u, abort_flag, p.status)) break;
+                // Launch start: every CTA would ask for its whole ring at once;
+                // the weights past the first D_FILL_GATE slots wait until the
+                // first slot has landed, so that each CTA's first slot is not
+                // queued behind the other CTAs' later ones.  (Slot 0 has
+                // completed at most its first phase here: its refill is pair NS.)
+                if (wprod && j == D_FILL_GATE && D_FILL_GATE < NS &&
+                    !wait_or_abort_lazy(BAR(full, 0), 0u, abort_flag, p.status))
+                    break;
                 const int nb2 = min(2, nblk - 2 * j);
                 const uint32_t st = ring + (uint32_t)s * SLOT;
                 if (wprod) {
