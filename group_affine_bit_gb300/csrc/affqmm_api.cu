@@ -231,7 +231,14 @@ int plan_prompt(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, Pr
         const int64_t tiles = (ws[i].N + kPromptTileN - 1) / kPromptTileN;
         P.tiles = (int32_t)tiles;
         P.units = (int32_t)(tiles * KB);
-        P.nctas = (int32_t)std::min<int64_t>(d.sms, P.units);
+        // Fewer tiles than SMs: every tile is cut into the same number S of
+        // depth runs and the grid is tiles x S CTAs, so that each run lies
+        // inside one tile (one segment, one partial, no pipeline drain in the
+        // middle of a run).  Otherwise one contiguous run of units per SM.
+        if (tiles < d.sms)
+            P.nctas = (int32_t)(tiles * std::min<int64_t>(d.sms / tiles, KB));
+        else
+            P.nctas = (int32_t)std::min<int64_t>(d.sms, P.units);
         P.cta_begin = (int32_t)ctas;
         P.ctr_begin = (int32_t)tiles_total;
         P.slot_begin = (int32_t)(2 * ctas);
