@@ -83,6 +83,12 @@ struct DecodePlan {
 // projection's (128-row tile, 128-deep block) units are cut into one run per
 // resident CTA (fewer if it has fewer units).  The cut of one projection does
 // not depend on the others in the launch.
+#if defined(AFFQMM_DECODE_ALIGN_PCT)
+constexpr int64_t kDecodeAlignPct = AFFQMM_DECODE_ALIGN_PCT;
+#else
+constexpr int64_t kDecodeAlignPct = 90;  // least share of resident CTAs a tile-aligned cut must fill
+#endif
+
 int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan) {
     std::memset(&plan->p, 0, sizeof(plan->p));
     const int64_t K = ws[0].K;
@@ -103,6 +109,12 @@ int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, De
         P.tiles = (int32_t)tiles;
         P.units = (int32_t)(tiles * KB);
         P.nctas = (int32_t)std::min<int64_t>(resident, P.units);
+        // Fewer tiles than resident CTAs, and a whole number of runs per tile
+        // still fills 90 % of them: every tile is cut into the same number of
+        // depth runs, so that each run lies inside one tile (one segment, one
+        // merge).  Otherwise one contiguous run of units per resident CTA.
+        if (tiles < resident && tiles * (resident / tiles) * 100 >= resident * kDecodeAlignPct)
+            P.nctas = (int32_t)(tiles * std::min<int64_t>(resident / tiles, KB));
         P.cta_begin = (int32_t)ctas;
         P.ctr_begin = (int32_t)tiles_total;
         P.slot_begin = (int32_t)(2 * ctas);

@@ -41,14 +41,20 @@ DECODE_CTAS_PER_SM = 2   # decode CTAs one SM holds (110 KB of shared memory eac
 
 def decode_tile_split(N: int, K: int, sms: int, ctas_per_sm: int = DECODE_CTAS_PER_SM):
     """How the decode launch cuts one projection: its (128-row tile, 128-deep
-    block) units, numbered tile-major, are cut into min(resident CTAs, units)
-    contiguous runs, run c = [c*U//PC, (c+1)*U//PC).  Returns (whole, split):
-    tiles that one run covers entirely (stored straight from registers) and
-    tiles that two or more runs share (fp32 partials merged in run order)."""
+    block) units, numbered tile-major, are cut into PC contiguous runs, run
+    c = [c*U//PC, (c+1)*U//PC), PC = min(resident CTAs, units) -- or, when
+    there are fewer tiles than resident CTAs and tiles x floor(resident /
+    tiles) fills 90 % of them, that many (every tile cut into the same number
+    of runs).  Returns (whole, split): tiles that one run covers entirely
+    (stored straight from registers) and tiles that two or more runs share
+    (fp32 partials merged in run order)."""
     tiles = -(-N // 128)
     KB = -(-K // 128)
     U = tiles * KB
-    PC = min(sms * ctas_per_sm, U)
+    resident = sms * ctas_per_sm
+    PC = min(resident, U)
+    if tiles < resident and tiles * (resident // tiles) * 10 >= resident * 9:
+        PC = tiles * min(resident // tiles, KB)
 
     def run_of(u):
         return ((u + 1) * PC - 1) // U
