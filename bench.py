@@ -51,7 +51,8 @@ L2_BYTES = 129 * 10 ** 6
 KERNEL_SOURCES = ["group_affine_bit_gb300/csrc/decode.cu", "group_affine_bit_gb300/csrc/prompt.cu",
                   "group_affine_bit_gb300/csrc/embed.cu",
                   "group_affine_bit_gb300/csrc/affqmm_format.cuh", "group_affine_bit_gb300/csrc/affqmm_tc.cuh",
-                  "group_affine_bit_gb300/csrc/affqmm_async.cuh"]
+                  "group_affine_bit_gb300/csrc/affqmm_async.cuh",
+                  "group_affine_bit_gb300/csrc/affqmm_api.cu"]   # the host planner: how a launch is cut
 
 
 # ----------------------------------------------------------------------------- setup
@@ -117,7 +118,8 @@ SHARED_KERNEL_HEADERS = KERNEL_SOURCES[3:]
 
 def source_digest(kernel: str | None = None) -> str:
     """Hash of the kernel sources: of one kernel ("decode", "prompt", "embed":
-    its .cu and the shared device headers), or of all of them."""
+    its .cu, the shared device headers and the host planner that cuts its
+    launches), or of all of them."""
     h = hashlib.sha256()
     rels = KERNEL_SOURCES if kernel is None else [f"group_affine_bit_gb300/csrc/{kernel}.cu", *SHARED_KERNEL_HEADERS]
     for rel in rels:

@@ -83,10 +83,17 @@ struct DecodePlan {
 // projection's (128-row tile, 128-deep block) units are cut into one run per
 // resident CTA (fewer if it has fewer units).  The cut of one projection does
 // not depend on the others in the launch.
+// Least share (%) of the resident CTAs that a tile-aligned cut must fill:
+// several runs per tile, or one whole tile per CTA (no merge at all).
 #if defined(AFFQMM_DECODE_ALIGN_PCT)
 constexpr int64_t kDecodeAlignPct = AFFQMM_DECODE_ALIGN_PCT;
 #else
-constexpr int64_t kDecodeAlignPct = 90;  // least share of resident CTAs a tile-aligned cut must fill
+constexpr int64_t kDecodeAlignPct = 90;
+#endif
+#if defined(AFFQMM_DECODE_WHOLE_PCT)
+constexpr int64_t kDecodeWholePct = AFFQMM_DECODE_WHOLE_PCT;
+#else
+constexpr int64_t kDecodeWholePct = 75;
 #endif
 
 int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan) {
@@ -109,12 +116,19 @@ int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, De
         P.tiles = (int32_t)tiles;
         P.units = (int32_t)(tiles * KB);
         P.nctas = (int32_t)std::min<int64_t>(resident, P.units);
-        // Fewer tiles than resident CTAs, and a whole number of runs per tile
-        // still fills 90 % of them: every tile is cut into the same number of
-        // depth runs, so that each run lies inside one tile (one segment, one
-        // merge).  Otherwise one contiguous run of units per resident CTA.
-        if (tiles < resident && tiles * (resident / tiles) * 100 >= resident * kDecodeAlignPct)
-            P.nctas = (int32_t)(tiles * std::min<int64_t>(resident / tiles, KB));
+        // Fewer tiles than resident CTAs: when a whole number S > 1 of runs
+        // per tile still fills 90 % of them, every tile is cut into S depth
+        // runs, so that each run lies inside one tile (one segment, one
+        // merge); when the tiles alone fill 75 %, each CTA takes one whole
+        // tile (no merge at all).  Otherwise one contiguous run of units per
+        // resident CTA ("stream-K").
+        if (tiles < resident) {
+            const int64_t S = std::min<int64_t>(resident / tiles, KB);
+            if (S > 1 && tiles * S * 100 >= resident * kDecodeAlignPct)
+                P.nctas = (int32_t)(tiles * S);
+            else if (tiles * 100 >= resident * kDecodeWholePct)
+                P.nctas = (int32_t)tiles;
+        }
         P.cta_begin = (int32_t)ctas;
         P.ctr_begin = (int32_t)tiles_total;
         P.slot_begin = (int32_t)(2 * ctas);

@@ -43,9 +43,9 @@ def decode_tile_split(N: int, K: int, sms: int, ctas_per_sm: int = DECODE_CTAS_P
     """How the decode launch cuts one projection: its (128-row tile, 128-deep
     block) units, numbered tile-major, are cut into PC contiguous runs, run
     c = [c*U//PC, (c+1)*U//PC), PC = min(resident CTAs, units) -- or, when
-    there are fewer tiles than resident CTAs and tiles x floor(resident /
-    tiles) fills 90 % of them, that many (every tile cut into the same number
-    of runs).  Returns (whole, split): tiles that one run covers entirely
+    there are fewer tiles than resident CTAs, tiles x S if S = floor(resident
+    / tiles) > 1 fills 90 % of them (every tile cut into S runs), else the
+    number of tiles if that fills 75 % (one whole tile per run).  Returns (whole, split): tiles that one run covers entirely
     (stored straight from registers) and tiles that two or more runs share
     (fp32 partials merged in run order)."""
     tiles = -(-N // 128)
@@ -53,8 +53,12 @@ def decode_tile_split(N: int, K: int, sms: int, ctas_per_sm: int = DECODE_CTAS_P
     U = tiles * KB
     resident = sms * ctas_per_sm
     PC = min(resident, U)
-    if tiles < resident and tiles * (resident // tiles) * 10 >= resident * 9:
-        PC = tiles * min(resident // tiles, KB)
+    if tiles < resident:
+        S = min(resident // tiles, KB)
+        if S > 1 and tiles * S * 100 >= resident * 90:
+            PC = tiles * S
+        elif tiles * 100 >= resident * 75:
+            PC = tiles
 
     def run_of(u):
         return ((u + 1) * PC - 1) // U
