@@ -9,6 +9,7 @@ over one batch of synthetic input with the weights resident in HBM:
   gate_up_decode (default)  M=1, K=3840, N=30720 (stacked gate/up), 4-bit g64
   decode_step               a 60-layer decoder's projections + tied head, M=1
   prompt_chunk              M=128 through one layer's four projection shapes
+  prompt_step               M=128 through all 60 layers' projections (the aggregate)
   lane_sweep                M in {2,4,8,16} at 4-bit g64 and M=16 at 8b/3b/2b
   tiny                      M=1, K=256, N=512, 4-bit g64
   embed_rows                4096 scaled embedding rows gathered from the tied head's table
@@ -62,8 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default: per workload)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="gate_up_decode",
-                    choices=["gate_up_decode", "decode_step", "prompt_chunk", "lane_sweep", "tiny", "embed_rows",
-                             "embed_rows_blocks", "gate_up_exact"])
+                    choices=["gate_up_decode", "decode_step", "prompt_chunk", "prompt_step", "lane_sweep", "tiny",
+                             "embed_rows", "embed_rows_blocks", "gate_up_exact"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -416,6 +417,32 @@ class PromptChunk(Workload):
         return f"{self.name}: M=128 through qkv, o, gate_up, down (hidden 5376), 4-bit group 64"
 
 
+class PromptStep(Workload):
+    """M = 128 activation rows through all 60 layers' four projections (every
+    weight distinct, 15.4 GB a step): the aggregate rate of a prompt chunk's
+    forward over the decoder."""
+    name = "prompt_step"
+    unit = "TFLOP/s"
+    default_steps = 100
+
+    def make_cases(self, api, synth, device):
+        c = synth.PROMPT_CHUNK
+        return [Case(api, synth, f"L{layer}.{label}", c["bits"], c["group"], c["M"], N, K,
+                     synth.step_seed(c["seed"], layer, j), 1, device)
+                for layer in range(synth.N_LAYERS)
+                for j, (label, (N, K)) in enumerate(synth.DECODER_LAYER_SHAPES.items())]
+
+    def describe(self):
+        return (f"{self.name}: M=128 through {len(self.cases) // 4} layers x (qkv, o, gate_up, down), hidden 5376, "
+                f"4-bit group 64, {len(self.cases)} projections")
+
+    def config(self):
+        d = super().config()
+        d["cases"] = d["cases"][:4] + [f"... {len(self.cases)} projections in all"]
+        d["packed_gb_per_step"] = round(sum(c.packed_bytes for c in self.cases) / 1e9, 3)
+        return d
+
+
 class LaneSweep(Workload):
     """M in {2, 4, 8, 16} at 4-bit g64 and M = 16 at 8-bit g32, 3-bit g64 and
     2-bit g128 on K = 3840, N = 15360."""
@@ -518,6 +545,7 @@ class EmbedRowsBlocks(EmbedRows):
 
 
 WORKLOADS = {"gate_up_decode": GateUpDecode, "decode_step": DecodeStep, "prompt_chunk": PromptChunk,
+             "prompt_step": PromptStep,
              "lane_sweep": LaneSweep, "tiny": Tiny, "embed_rows": EmbedRows, "embed_rows_blocks": EmbedRowsBlocks,
              "gate_up_exact": GateUpExact}
 
@@ -739,6 +767,8 @@ WORKLOAD_ORACLE_SHAPES = {   # the projection each workload's oracle sample take
                                   K=s.DECODER_LAYER_SHAPES["gate_up"][1], seed=s.step_seed(s.DECODE_STEP_SEED, 0, 2)),
     "prompt_chunk": lambda s: dict(bits=4, group=64, M=128, N=s.DECODER_LAYER_SHAPES["qkv"][0],
                                    K=s.DECODER_LAYER_SHAPES["qkv"][1], seed=s.step_seed(s.PROMPT_CHUNK["seed"], 0, 0)),
+    "prompt_step": lambda s: dict(bits=4, group=64, M=128, N=s.DECODER_LAYER_SHAPES["qkv"][0],
+                                  K=s.DECODER_LAYER_SHAPES["qkv"][1], seed=s.step_seed(s.PROMPT_CHUNK["seed"], 0, 0)),
     "lane_sweep": lambda s: dict(bits=4, group=64, M=2, N=s.SWEEP_SHAPE["N"], K=s.SWEEP_SHAPE["K"],
                                  seed=s.SWEEP_SHAPE["seed"]),
     "embed_rows": lambda s: dict(bits=4, group=64, M=1, N=4096, K=s.HEAD_SHAPE[1], seed=s.EMBED_SEED, embed=True),
@@ -861,11 +891,15 @@ def main(argv=None):
                                     "seconds": round(dt1, 2)}
 
     if rank == 0:
+        codes_only = None   # the same rate counting the code bytes alone (no scales and biases)
+        if wl.unit == "GB/s" and getattr(wl, "cases", None):
+            codes_only = value * sum(c.N * c.K * c.bits // 8 for c in wl.cases) / sum(c.packed_bytes for c in wl.cases)
         line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world, "steps": steps,
                 "warmup": warmup, "ms_per_step": t_max / steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": wl.config(), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": steps * wl.kernels_per_step, "clocks": clocks, "kernel_src_digest": source_digest()}
+                "gpu_launches": steps * wl.kernels_per_step, "clocks": clocks, "kernel_src_digest": source_digest(),
+                "codes_only_gbs": codes_only}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
