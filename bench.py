@@ -271,6 +271,32 @@ class Workload:
         self.api = api
         self.workspace = api.Workspace(device)
         self.cases = self.make_cases(api, synth, device)
+        self.x_arena = self.y_arena = None
+        if len(self.cases) > 1:
+            self._arenas(device)
+
+    def _arenas(self, device):
+        """A step's activations and outputs in one contiguous buffer each (the
+        cases' x and y become views of them, 16-byte aligned, same values), as
+        an engine keeps a step's activations: the step's inputs go up in one
+        copy and its outputs come back in one."""
+        import torch
+
+        def carve(shapes):
+            offs, n = [], 0
+            for rows, cols in shapes:
+                offs.append(n)
+                n += -(-rows * cols // 8) * 8          # 16-byte aligned views
+            return offs, n
+        xo, xn = carve([(c.M, c.K) for c in self.cases])
+        yo, yn = carve([(c.M, c.N) for c in self.cases])
+        self.x_arena = torch.empty(xn, dtype=torch.bfloat16, device=device)
+        self.y_arena = torch.empty(yn, dtype=torch.bfloat16, device=device)
+        for c, a, b in zip(self.cases, xo, yo):
+            xv = self.x_arena[a:a + c.M * c.K].view(c.M, c.K)
+            xv.copy_(c.x)
+            c.x = xv
+            c.y = self.y_arena[b:b + c.M * c.N].view(c.M, c.N)
 
     def make_cases(self, api, synth, device):
         raise NotImplementedError
@@ -327,6 +353,8 @@ class Workload:
             "l2": self.l2_note(), "parallelism": "replicas"}
 
     def e2e_io(self):
+        if self.x_arena is not None:
+            return [self.x_arena], [self.y_arena]
         return [c.x for c in self.cases], [c.y for c in self.cases]
 
     def oracle_shape(self):
