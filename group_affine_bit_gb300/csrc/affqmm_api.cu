@@ -187,6 +187,21 @@ Fn driver_fn(const char* name) {
         return nullptr;
     return reinterpret_cast<Fn>(f);
 }
+// The GPU's address of page-locked host memory, or NULL for any other memory
+// (pageable host memory, device memory, an unknown pointer).
+using PointerAttrFn = CUresult (*)(void*, CUpointer_attribute, CUdeviceptr);
+const void* host_on_device(const void* p) {
+    static PointerAttrFn get = driver_fn<PointerAttrFn>("cuPointerGetAttribute");
+    if (!get || !p) return nullptr;
+    unsigned int type = 0;
+    if (get(&type, CU_POINTER_ATTRIBUTE_MEMORY_TYPE, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS ||
+        type != CU_MEMORYTYPE_HOST)
+        return nullptr;
+    CUdeviceptr d = 0;
+    if (get(&d, CU_POINTER_ATTRIBUTE_DEVICE_POINTER, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return nullptr;
+    return reinterpret_cast<const void*>(d);
+}
+
 CopyHtoDFn copy_htod() {
     static CopyHtoDFn fn = driver_fn<CopyHtoDFn>("cuMemcpyHtoDAsync");
     return fn;
@@ -648,16 +663,27 @@ int affqmm_run_host(const affqmm_weight* w, const uint16_t* x, int64_t M, uint16
     // every check of the device call (x_dev, y_dev, workspace, device) before anything is enqueued
     rc = run_impl(1, w, x_dev, M, ys, workspace, ws_bytes, stream, Form(), true);
     if (rc) return rc;
+    const size_t xbytes = (size_t)M * (size_t)w->K * 2, ybytes = (size_t)M * (size_t)w->N * 2;
+    // Page-locked host buffers: the transfers run as kernels chained to the
+    // projection (hostio.cu), so that no copy sits between two launches.
+    const void* x_gpu = w->K > 0 ? host_on_device(x) : nullptr;
+    void* y_gpu = const_cast<void*>(host_on_device(y));
+    if ((w->K == 0 || x_gpu) && y_gpu) {
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        if (w->K > 0 && launch_host_upload(x_gpu, x_dev, xbytes, st) != cudaSuccess) return AFFQMM_E_CUDA;
+        rc = run_impl(1, w, x_dev, M, ys, workspace, ws_bytes, stream);
+        if (rc) return rc;
+        if (launch_host_download(y_dev, y_gpu, ybytes, st) != cudaSuccess) return AFFQMM_E_CUDA;
+        return AFFQMM_OK;
+    }
     CopyHtoDFn htod = copy_htod();
     CopyDtoHFn dtoh = copy_dtoh();
     if (!htod || !dtoh) return AFFQMM_E_CUDA;
     CUstream cs = static_cast<CUstream>(stream);
-    if (w->K > 0 && htod(reinterpret_cast<CUdeviceptr>(x_dev), x, (size_t)M * (size_t)w->K * 2, cs) != CUDA_SUCCESS)
-        return AFFQMM_E_CUDA;
+    if (w->K > 0 && htod(reinterpret_cast<CUdeviceptr>(x_dev), x, xbytes, cs) != CUDA_SUCCESS) return AFFQMM_E_CUDA;
     rc = run_impl(1, w, x_dev, M, ys, workspace, ws_bytes, stream);
     if (rc) return rc;
-    if (dtoh(y, reinterpret_cast<CUdeviceptr>(y_dev), (size_t)M * (size_t)w->N * 2, cs) != CUDA_SUCCESS)
-        return AFFQMM_E_CUDA;
+    if (dtoh(y, reinterpret_cast<CUdeviceptr>(y_dev), ybytes, cs) != CUDA_SUCCESS) return AFFQMM_E_CUDA;
     return AFFQMM_OK;
 }
 

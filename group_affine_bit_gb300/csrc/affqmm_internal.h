@@ -133,5 +133,9 @@ cudaError_t launch_embed(int bits, int group, bool rowcopy, const void* table, i
                          cudaStream_t st);
 cudaError_t launch_pack_rows(int bits, int group, const void* packed, int64_t N, int64_t K, void* rows,
                              cudaStream_t st);
+// hostio.cu: the host-buffer entry point's transfers as kernels (the host
+// pointers are the GPU's addresses of page-locked host memory).
+cudaError_t launch_host_upload(const void* host_src, void* dev_dst, size_t bytes, cudaStream_t st);
+cudaError_t launch_host_download(const void* dev_src, void* host_dst, size_t bytes, cudaStream_t st);
 
 }  // namespace affqmm

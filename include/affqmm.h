@@ -241,8 +241,12 @@ AFFQMM_API int affqmm_run_stacked(int count, const affqmm_weight* ws, const uint
 /* affqmm_run with the activations and outputs in host memory, the whole
  * step of a caller that keeps x and y on the host: x is copied into x_dev,
  * the projection runs, y_dev is copied back into y -- all enqueued on
- * `stream` in that order (cudaMemcpyAsync, one copy each way).
- *   x        host, bf16 [M, K] row-major (page-locked memory keeps the copy
+ * `stream` in that order.  When x and y are page-locked host memory (which
+ * the GPU can address), both transfers are small kernels chained to the
+ * projection: x is read from host memory while the previous kernel in the
+ * stream finishes, and y is written to host memory as soon as the projection
+ * has finished.  Otherwise the driver's asynchronous copies move them.
+ *   x        host, bf16 [M, K] row-major (page-locked memory keeps the call
  *            asynchronous; pageable memory works and makes it synchronous)
  *   y        host, bf16 [M, N] row-major; complete once the stream reaches
  *            the end of the call
