@@ -53,7 +53,7 @@ KERNEL_SOURCES = ["group_affine_bit_gb300/csrc/decode.cu", "group_affine_bit_gb3
                   "group_affine_bit_gb300/csrc/embed.cu",
                   "group_affine_bit_gb300/csrc/affqmm_format.cuh", "group_affine_bit_gb300/csrc/affqmm_tc.cuh",
                   "group_affine_bit_gb300/csrc/affqmm_async.cuh",
-                  "group_affine_bit_gb300/csrc/affqmm_api.cu"]   # the host planner: how a launch is cut
+                  "group_affine_bit_gb300/csrc/plan.cu"]   # the host planner: how a launch is cut
 
 
 # ----------------------------------------------------------------------------- setup

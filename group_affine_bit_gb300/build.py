@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libaffqmm.so")
 
-SOURCES = ["affqmm_api.cu", "pack.cu", "decode.cu", "prompt.cu", "embed.cu", "hostio.cu"]
+SOURCES = ["affqmm_api.cu", "plan.cu", "pack.cu", "decode.cu", "prompt.cu", "embed.cu", "hostio.cu"]
 HEADERS = ["affqmm_format.cuh", "affqmm_internal.h", "affqmm_async.cuh", "affqmm_tc.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

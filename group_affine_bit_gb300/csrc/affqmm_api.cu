@@ -73,74 +73,6 @@ int check_weight(const affqmm_weight* w) {
     return AFFQMM_OK;
 }
 
-struct DecodePlan {
-    DecParams p;
-    int grid = 0;
-    size_t ws_bytes = 0;
-};
-
-// Decomposition of a decode launch over `count` projections (M <= 16): each
-// projection's (128-row tile, 128-deep block) units are cut into one run per
-// resident CTA (fewer if it has fewer units).  The cut of one projection does
-// not depend on the others in the launch.
-// Least share (%) of the resident CTAs that a tile-aligned cut must fill:
-// several runs per tile, or one whole tile per CTA (no merge at all).
-#if defined(AFFQMM_DECODE_ALIGN_PCT)
-constexpr int64_t kDecodeAlignPct = AFFQMM_DECODE_ALIGN_PCT;
-#else
-constexpr int64_t kDecodeAlignPct = 90;
-#endif
-#if defined(AFFQMM_DECODE_WHOLE_PCT)
-constexpr int64_t kDecodeWholePct = AFFQMM_DECODE_WHOLE_PCT;
-#else
-constexpr int64_t kDecodeWholePct = 75;
-#endif
-
-int plan_decode(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan) {
-    std::memset(&plan->p, 0, sizeof(plan->p));
-    const int64_t K = ws[0].K;
-    const int KB = (int)((K + KBLK - 1) / KBLK);
-    DecParams& p = plan->p;
-    p.nproj = count;
-    p.KB = KB;
-    p.K = K;
-    p.M = (int32_t)M;
-    p.fault_wait = decode_fault_wait();
-    const int64_t resident = (int64_t)d.sms * d.dec_ctas_per_sm;
-    int64_t ctas = 0, tiles_total = 0;
-    for (int i = 0; i < count; ++i) {
-        DecProj& P = p.proj[i];
-        P.N = ws[i].N;
-        P.packed = static_cast<const uint8_t*>(ws[i].packed);
-        const int64_t tiles = (ws[i].N + TILE_N - 1) / TILE_N;
-        P.tiles = (int32_t)tiles;
-        P.units = (int32_t)(tiles * KB);
-        P.nctas = (int32_t)std::min<int64_t>(resident, P.units);
-        // Fewer tiles than resident CTAs: when a whole number S > 1 of runs
-        // per tile still fills 90 % of them, every tile is cut into S depth
-        // runs, so that each run lies inside one tile (one segment, one
-        // merge); when the tiles alone fill 75 %, each CTA takes one whole
-        // tile (no merge at all).  Otherwise one contiguous run of units per
-        // resident CTA ("stream-K").
-        if (tiles < resident) {
-            const int64_t S = std::min<int64_t>(resident / tiles, KB);
-            if (S > 1 && tiles * S * 100 >= resident * kDecodeAlignPct)
-                P.nctas = (int32_t)(tiles * S);
-            else if (tiles * 100 >= resident * kDecodeWholePct)
-                P.nctas = (int32_t)tiles;
-        }
-        P.cta_begin = (int32_t)ctas;
-        P.ctr_begin = (int32_t)tiles_total;
-        P.slot_begin = (int32_t)(2 * ctas);
-        ctas += P.nctas;
-        tiles_total += tiles;
-    }
-    if (kDecCountersPerTile * tiles_total > (int64_t)kMaxCounters) return AFFQMM_E_SHAPE;
-    plan->grid = (int)ctas;
-    plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kDecSlotFloats * sizeof(float) : 0;
-    return AFFQMM_OK;
-}
-
 void bind_workspace(DecodePlan* plan, void* workspace) {
     if (plan->ws_bytes == 0) return;
     uint8_t* base = static_cast<uint8_t*>(workspace);
@@ -149,11 +81,6 @@ void bind_workspace(DecodePlan* plan, void* workspace) {
     plan->p.partials = reinterpret_cast<float*>(base + kSlotsOffset);
 }
 
-// Rows per launch: the decode kernel takes up to 16 activation rows, the
-// prompt kernel up to 128.
-constexpr int64_t kDecodeRows = 16;
-constexpr int64_t kPromptRows = 128;
-constexpr int kPromptTileN = 256;
 
 // cuTensorMapEncodeTiled, fetched from the driver at run time.
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -243,55 +170,6 @@ int make_x_map_decode(const uint16_t* x, int64_t M, int64_t K, CUtensorMap* map)
     return r == CUDA_SUCCESS ? AFFQMM_OK : AFFQMM_E_CUDA;
 }
 
-struct PromptPlan {
-    PromptParams p;
-    int grid = 0;
-    size_t ws_bytes = 0;
-};
-
-// Decomposition of a prompt launch: each projection's (256-row tile, block)
-// units are cut into one run per SM (fewer if it has fewer units).
-int plan_prompt(DeviceInfo& d, int count, const affqmm_weight* ws, int64_t M, PromptPlan* plan) {
-    std::memset(&plan->p, 0, sizeof(plan->p));
-    PromptParams& p = plan->p;
-    const int bits = ws[0].bits, group = ws[0].group;
-    const int64_t K = ws[0].K;
-    const int KB = (int)((K + KBLK - 1) / KBLK);
-    p.nproj = count;
-    p.KB = KB;
-    p.K = K;
-    p.M = (int32_t)M;
-    p.block_bytes = block_bytes(bits, group);
-    p.group = group;
-    int64_t ctas = 0, tiles_total = 0;
-    for (int i = 0; i < count; ++i) {
-        PromptProj& P = p.proj[i];
-        P.N = ws[i].N;
-        P.packed = static_cast<const uint8_t*>(ws[i].packed);
-        P.ltiles = (int32_t)((ws[i].N + TILE_N - 1) / TILE_N);
-        const int64_t tiles = (ws[i].N + kPromptTileN - 1) / kPromptTileN;
-        P.tiles = (int32_t)tiles;
-        P.units = (int32_t)(tiles * KB);
-        // Fewer tiles than SMs: every tile is cut into the same number S of
-        // depth runs and the grid is tiles x S CTAs, so that each run lies
-        // inside one tile (one segment, one partial, no pipeline drain in the
-        // middle of a run).  Otherwise one contiguous run of units per SM.
-        if (tiles < d.sms)
-            P.nctas = (int32_t)(tiles * std::min<int64_t>(d.sms / tiles, KB));
-        else
-            P.nctas = (int32_t)std::min<int64_t>(d.sms, P.units);
-        P.cta_begin = (int32_t)ctas;
-        P.ctr_begin = (int32_t)tiles_total;
-        P.slot_begin = (int32_t)(2 * ctas);
-        ctas += P.nctas;
-        tiles_total += tiles;
-    }
-    if (tiles_total > 65535) return AFFQMM_E_SHAPE;  // one merge-kernel grid row per 256-row tile
-    plan->grid = (int)ctas;
-    plan->ws_bytes = ctas > 0 ? kSlotsOffset + (size_t)(2 * ctas) * kPromptSlotFloats * sizeof(float) : 0;
-    return AFFQMM_OK;
-}
-
 int workspace_for(int count, const affqmm_weight* ws, int64_t M, size_t* bytes) {
     DeviceInfo* d = nullptr;
     int rc = device_info(&d);
@@ -300,12 +178,12 @@ int workspace_for(int count, const affqmm_weight* ws, int64_t M, size_t* bytes) 
     if (M == 0) return AFFQMM_OK;
     if (M <= kDecodeRows) {
         DecodePlan plan;
-        rc = plan_decode(*d, count, ws, M, &plan);
+        rc = plan_decode(d->sms, d->dec_ctas_per_sm, count, ws, M, &plan);
         if (rc) return rc;
         *bytes = plan.ws_bytes;
     } else {
         PromptPlan plan;
-        rc = plan_prompt(*d, count, ws, std::min<int64_t>(M, kPromptRows), &plan);
+        rc = plan_prompt(d->sms, count, ws, std::min<int64_t>(M, kPromptRows), &plan);
         if (rc) return rc;
         *bytes = plan.ws_bytes;
     }
@@ -443,7 +321,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         CachedLaunch* c = find_launch(key);
         if (!c) {
             DecodePlan plan;
-            rc = plan_decode(*d, count, ws, M, &plan);
+            rc = plan_decode(d->sms, d->dec_ctas_per_sm, count, ws, M, &plan);
             if (rc) return rc;
             rc = check_workspace(plan.ws_bytes, workspace, ws_bytes);
             if (rc) return rc;
@@ -472,7 +350,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
         CachedLaunch* c = find_launch(key);
         if (!c) {
             PromptPlan plan;
-            rc = plan_prompt(*d, count, ws, M, &plan);
+            rc = plan_prompt(d->sms, count, ws, M, &plan);
             if (rc) return rc;
             rc = check_workspace(plan.ws_bytes, workspace, ws_bytes);
             if (rc) return rc;
@@ -498,7 +376,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
     // The first chunk is the largest: its plan sizes the workspace.
     {
         PromptPlan first;
-        rc = plan_prompt(*d, count, ws, std::min<int64_t>(M, kPromptRows), &first);
+        rc = plan_prompt(d->sms, count, ws, std::min<int64_t>(M, kPromptRows), &first);
         if (rc) return rc;
         rc = check_workspace(first.ws_bytes, workspace, ws_bytes);
         if (rc || dry) return rc;
@@ -507,7 +385,7 @@ int run_impl(int count, const affqmm_weight* ws, const uint16_t* x, int64_t M, u
     for (int64_t m0 = 0; m0 < M; m0 += kPromptRows) {
         const int64_t mc = std::min(kPromptRows, M - m0);
         PromptPlan plan;
-        rc = plan_prompt(*d, count, ws, mc, &plan);
+        rc = plan_prompt(d->sms, count, ws, mc, &plan);
         if (rc) return rc;
         plan.p.status = reinterpret_cast<uint32_t*>(wsb);
         plan.p.counters = reinterpret_cast<uint32_t*>(wsb + kStatusBytes);
@@ -820,7 +698,7 @@ extern "C" int affqmm_run_noalloc(const affqmm_weight* w, const uint16_t* x, int
         return cudaMemsetAsync(y, 0, (size_t)M * w->N * 2, st) == cudaSuccess ? AFFQMM_OK : AFFQMM_E_CUDA;
     }
     DecodePlan plan;
-    rc = plan_decode(*d, 1, w, M, &plan);
+    rc = plan_decode(d->sms, d->dec_ctas_per_sm, 1, w, M, &plan);
     if (rc) return rc;
     if (plan.ws_bytes > sizeof(g_noalloc_scratch)) return AFFQMM_E_SCRATCH;
     void* scratch = nullptr;

@@ -133,6 +133,25 @@ cudaError_t launch_embed(int bits, int group, bool rowcopy, const void* table, i
                          cudaStream_t st);
 cudaError_t launch_pack_rows(int bits, int group, const void* packed, int64_t N, int64_t K, void* rows,
                              cudaStream_t st);
+// plan.cu: how a launch is cut (see there).  Rows per launch: the decode
+// kernel takes up to 16 activation rows, the prompt kernel up to 128; a prompt
+// unit covers 256 weight rows.
+constexpr int64_t kDecodeRows = 16;
+constexpr int64_t kPromptRows = 128;
+constexpr int kPromptTileN = 256;
+struct DecodePlan {
+    DecParams p;
+    int grid = 0;
+    size_t ws_bytes = 0;
+};
+struct PromptPlan {
+    PromptParams p;
+    int grid = 0;
+    size_t ws_bytes = 0;
+};
+int plan_decode(int sms, int ctas_per_sm, int count, const affqmm_weight* ws, int64_t M, DecodePlan* plan);
+int plan_prompt(int sms, int count, const affqmm_weight* ws, int64_t M, PromptPlan* plan);
+
 // hostio.cu: the host-buffer entry point's transfers as kernels (the host
 // pointers are the GPU's addresses of page-locked host memory).
 cudaError_t launch_host_upload(const void* host_src, void* dev_dst, size_t bytes, cudaStream_t st);
