@@ -610,6 +610,11 @@ def time_steps(wl, steps: int, warmup: int, dist, device):
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize(device)
+    # Keep the GPU busy (a spin of ~0.1 ms) while the host enqueues the start
+    # event and the graphs, so that the timed region starts when the GPU
+    # reaches the work, not when the host finishes submitting it.
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(200_000)
     e0.record(stream)
     for _ in range(steps // chunk):
         full.replay()
