@@ -35,7 +35,7 @@ def test_cached_setups_follow_every_argument(M):
     wss = [api.Workspace(), api.Workspace()]
     combos = [(wi, xi, wsi) for wi in range(3) for xi in range(3) for wsi in range(2)]
     first = {}
-    for rnd in range(2):
+    for pas in range(2):
         for (wi, xi, wsi) in combos:
             y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
             api.run(weights[wi], xs[xi], y=y, workspace=wss[wsi])
@@ -43,7 +43,7 @@ def test_cached_setups_follow_every_argument(M):
             assert not torch.isnan(y.float()).any(), f"output not written for {(wi, xi, wsi)}"
             key = (wi, xi)
             if key in first:
-                assert torch.equal(bits16(y), first[key]), f"round {rnd}: {(wi, xi, wsi)} differs"
+                assert torch.equal(bits16(y), first[key]), f"pass {pas}: {(wi, xi, wsi)} differs"
             else:
                 first[key] = bits16(y)
     # distinct weights and inputs give distinct outputs (the cache never served another call's set-up)
