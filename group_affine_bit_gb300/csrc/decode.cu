@@ -49,7 +49,7 @@
 // same inputs give the same bits on every call, alone or stacked.  Every
 // wait is on an mbarrier with a bound; a wait that gives up sets the
 // workspace status word and an abort flag, and every role finishes.
-// Prior art: the "reg variant" lane projection of the "Gemma 4 12B on the
+// Prior art: the reg variant of the lane projection on the "Gemma 4 12B on the
 // native Metal engine" page (4-bit groups held in registers for the
 // matrix-op, K split per shape); unlike it, every weight is rounded to bf16
 // before the contraction, as that page's prompt GEMM does.

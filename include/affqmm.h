@@ -10,15 +10,16 @@
  *   - q are integer codes of `bits` bits (2, 3, 4, 5, 6 or 8) with one bf16
  *     scale s and one bf16 bias b per group of g = 32, 64 or 128 consecutive
  *     k of a row: "cuda gemma4: images on the 12B" page, the embed_rows
- *     commit ("MLX's affine tables at 2, 3, 4, 5, 6 or 8 bits (groups of 32,
- *     64 or 128)"), and the widths commit of the same page (AffineN tiles).
+ *     commit (MLX's affine tables at those widths and group sizes), and the
+ *     widths commit of the same page (AffineN tiles).
  *   - each weight is rounded once, bf16(fma(s, q, b)), and the products are
  *     accumulated over the whole depth: "Gemma 4 12B on the native Metal
- *     engine" page, the commit where the prompt tiles dequantize "as mlx-lm's
- *     quantized matmul dequantizes".
+ *     engine" page, the commit where the prompt tiles dequantize each weight
+ *     the way mlx-lm's quantized matmul does.
  *   - M = 1..16 activation rows (decode lanes) run a memory-bound kernel;
  *     M >= 17 runs the tcgen05 tensor-core kernel in chunks of up to 128 rows
- *     (prompt chunks: the same page's "128 rows in one weight read").
+ *     (prompt chunks: the same page's commit that runs a window's 128 rows on
+ *     one read of the weights).
  *
  * Conventions for every entry point:
  *   - Device pointers are CUDA device (or managed) memory of the current
@@ -203,9 +204,10 @@ AFFQMM_API int affqmm_run_exact_sums(const affqmm_weight* w, const uint16_t* x, 
 #define AFFQMM_FORM_EXACT_SUMS 2  /* exact codes with the caller's group sums, as affqmm_run_exact_sums */
 
 /* A gate/up stack with GeGLU as its epilogue ("Gemma 4 12B on the native
- * Metal engine" page: geglu as the gate/up projection's epilogue, the stack's
- * rows interleaved in 16-row blocks, the same bits as apart; "cuda gemma4"
- * page: mlx_lm's gelu_approx(gate) * up as MLX's bf16 operations).
+ * Metal engine" page: geglu fused into the gate/up projection's epilogue,
+ * the stack's rows interleaved in 16-row blocks, the fused results equal to
+ * the unfused ones; "cuda gemma4" page: mlx_lm's gelu_approx(gate) * up as
+ * MLX's bf16 operations).
  *   w      the stack, N = 2F rows interleaved in 16-row blocks: rows
  *          32j .. 32j + 15 are gate rows 16j .. 16j + 15, rows 32j + 16 ..
  *          32j + 31 the up rows of the same hidden units; N % 32 == 0
@@ -226,7 +228,7 @@ AFFQMM_API int affqmm_run_geglu(const affqmm_weight* w, const uint16_t* x, const
 /* Several projections of the same x in one launch: a layer's q/k/v or
  * gate/up stack ("Gemma 4 12B on the native Metal engine" page, the commit
  * that packs each layer's q/k/v, o, gate/up and down stacks and the tied
- * head once: seven shapes).
+ * head once, so that a layer runs on a handful of packed shapes).
  *   ws      host array of `count` weight views (1 <= count <= AFFQMM_MAX_STACK)
  *           with equal K, bits and group, passed by value in one array (the
  *           views are small structs; an array of them is what the caller

@@ -19,7 +19,7 @@
  *    the prompt GEMM dequantize each weight as bf16(fma(scale, code, bias)) with
  *    one rounding, as mlx-lm's quantized matmul does, and accumulate over the
  *    whole depth; the same page's lane kernels that keep codes exact and use
- *    precomputed group sums (the "reg variant" commit).
+ *    precomputed group sums (the commit on the reg variant of the lane kernel).
  *  - "cuda gemma4: images on the 12B ..." (PR #1183), the embed_rows commit
  *    (MLX affine tables at 2/3/4/5/6/8 bits, groups of 32/64/128) and the
  *    bf16 rounding commit (signed zero from underflow, subnormal ties, the
@@ -90,7 +90,7 @@ int oracle_qmm_groupsum_given(int bits, int group, int64_t M, int64_t N, int64_t
  *   r  = bf16(p * e)      h  = bf16(r * up)
  * ("cuda gemma4" page: tf_geglu_rows computes mlx_lm's gelu_approx(gate) * up
  * as MLX's bf16 ops; "Gemma 4 12B on the native Metal engine" page: geglu as
- * the gate/up projection's epilogue, the same bits as apart).  tanh is the
+ * the gate/up projection's epilogue, its results equal to the unfused ones).  tanh is the
  * double library function.  A GPU's fp32 tanh is within `tanh_ulps` fp32
  * ulps of the exact value, so where the exact tanh lies that close to a bf16
  * rounding boundary the bf16 t has two possible values: h_lo takes the one

@@ -8,7 +8,7 @@
   blocks, with GeGLU (mlx_lm's gelu_approx(gate) * up as bf16 operations) as
   the projection's epilogue.  Its output must have the bits of the unfused
   projection followed by the oracle's GeGLU on that projection's own bf16
-  outputs ("the same bits as apart"), up to the one bf16 step an fp32 tanh
+  outputs (fusing changes no bit), up to the one bf16 step an fp32 tanh
   within a few ulps may move (the oracle returns both candidates), for the
   rounded, exact-codes and producer-sums forms.
 """
