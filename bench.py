@@ -627,6 +627,32 @@ def time_steps(wl, steps: int, warmup: int, dist, device):
     return seconds, (full, rest, chunk)
 
 
+def time_cases(wl, device, launches: int = 40, replays: int = 5):
+    """Rate of each case of a few-case workload timed alone (graph replay of
+    `launches` launches over its rotating copies, CUDA events): the per-case
+    figures beside the step's aggregate."""
+    import torch
+    out = {}
+    stream = torch.cuda.current_stream(device)
+    for c in wl.cases:
+        g = graph_of(lambda i, c=c: c.run(i, wl.workspace), 0, launches)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        sec = e0.elapsed_time(e1) * 1e-3 / (launches * replays)
+        units = c.flops if wl.unit == "TFLOP/s" else c.packed_bytes
+        out[c.label] = round(units / sec / wl.scale, 1)
+        del g
+    return out
+
+
 def sustain_for_clocks(graphs, device, seconds: float = 1.0):
     """Replay the timed graphs for about `seconds` so the clock sampler sees
     the same load when the timed region itself is too short to sample."""
@@ -924,13 +950,16 @@ def main(argv=None):
                                     "seconds": round(dt1, 2)}
 
     if rank == 0:
+        config = wl.config()
+        if 1 < len(getattr(wl, "cases", [])) <= 8 and world == 1:
+            config["per_case_" + wl.unit.replace("/", "")] = time_cases(wl, device)
         codes_only = None   # the same rate counting the code bytes alone (no scales and biases)
         if wl.unit == "GB/s" and getattr(wl, "cases", None):
             codes_only = value * sum(c.N * c.K * c.bits // 8 for c in wl.cases) / sum(c.packed_bytes for c in wl.cases)
         line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world, "steps": steps,
                 "warmup": warmup, "ms_per_step": t_max / steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": wl.config(), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": steps * wl.kernels_per_step, "clocks": clocks, "kernel_src_digest": source_digest(),
                 "codes_only_gbs": codes_only}
         print(json.dumps(line), flush=True)
