@@ -48,7 +48,7 @@ int plan_decode(int sms, int ctas_per_sm, int count, const affqmm_weight* ws, in
         // merge); when the tiles alone fill 75 %, each CTA takes one whole
         // tile (no merge at all).  Otherwise one contiguous run of units per
         // resident CTA ("stream-K").
-        if (tiles < resident) {
+        if (tiles > 0 && tiles < resident) {
             const int64_t S = std::min<int64_t>(resident / tiles, KB);
             if (S > 1 && tiles * S * 100 >= resident * kDecodeAlignPct)
                 P.nctas = (int32_t)(tiles * S);
@@ -97,7 +97,7 @@ int plan_prompt(int sms, int count, const affqmm_weight* ws, int64_t M, PromptPl
         // depth runs and the grid is tiles x S CTAs, so that each run lies
         // inside one tile (one segment, one partial, no pipeline drain in the
         // middle of a run).  Otherwise one contiguous run of units per SM.
-        if (tiles < sms)
+        if (tiles > 0 && tiles < sms)
             P.nctas = (int32_t)(tiles * std::min<int64_t>(sms / tiles, KB));
         else
             P.nctas = (int32_t)std::min<int64_t>(sms, P.units);

@@ -349,7 +349,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 // row m (a 16-byte load from each run's partial: a warp reads 512 contiguous
 // bytes), so the whole merge is a few rounds of fully parallel L2 reads.
 // Tiles that one run owned were stored by prompt_kernel and are skipped.
+// RB runs' loads are issued before they are added: 4, or 8 for launches whose
+// tiles have more than four runs (every partial of a 7-run tile in one round
+// of loads; with few runs the wider body costs more than it saves).
 constexpr int P_MERGE_THREADS = 256;
+template <int RB>
 __global__ void __launch_bounds__(P_MERGE_THREADS) prompt_merge_kernel(const __grid_constant__ PromptParams p) {
     pdl_launch_dependents();  // the next kernel's prologue and weight copies may start
     pdl_wait();               // the partials of prompt_kernel are complete and visible
@@ -368,16 +372,25 @@ __global__ void __launch_bounds__(P_MERGE_THREADS) prompt_merge_kernel(const __g
     const int64_t n = (int64_t)tile * P_TILE_N + n4;
     if (m >= p.M || n >= P.N) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int cb = cf; cb <= cl; ++cb) {
-        const int b0 = (int)((int64_t)cb * U / PC);
-        const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
-        const float4 f = __ldcg(
-            reinterpret_cast<const float4*>(p.slots + (size_t)sc * kPromptSlotFloats + (size_t)m * P_TILE_N + n4));
-        acc.x += f.x;
-        acc.y += f.y;
-        acc.z += f.z;
-        acc.w += f.w;
+    for (int cb0 = cf; cb0 <= cl; cb0 += RB) {
+        float4 f[RB];
+#pragma unroll
+        for (int d = 0; d < RB; ++d) {
+            const int cb = cb0 + d;
+            if (cb > cl) break;
+            const int b0 = (int)((int64_t)cb * U / PC);
+            const int sc = P.slot_begin + 2 * cb + (b0 >= t0 ? 0 : 1);
+            f[d] = __ldcg(
+                reinterpret_cast<const float4*>(p.slots + (size_t)sc * kPromptSlotFloats + (size_t)m * P_TILE_N + n4));
+        }
+#pragma unroll
+        for (int d = 0; d < RB; ++d) {
+            if (cb0 + d > cl) break;
+            acc.x += f[d].x;
+            acc.y += f[d].y;
+            acc.z += f[d].z;
+            acc.w += f[d].w;
+        }
     }
     uint16_t* yr = P.y + (int64_t)m * P.N + n;
     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
@@ -397,7 +410,11 @@ cudaError_t launch_prompt_bg(const PromptParams& p, const CUtensorMap& map, int 
     if (e != cudaSuccess) return e;
     const PromptProj& last = p.proj[p.nproj - 1];
     const dim3 mgrid((unsigned)((p.M + 3) / 4), (unsigned)(last.ctr_begin + last.tiles));
-    return launch_pdl(prompt_merge_kernel, mgrid, P_MERGE_THREADS, 0, st, p);
+    int runs = 0;  // most runs sharing one tile in this launch (a bound)
+    for (int i = 0; i < p.nproj; ++i)
+        if (p.proj[i].tiles > 0) runs = max(runs, (p.proj[i].nctas + p.proj[i].tiles - 1) / p.proj[i].tiles + 1);
+    if (runs > 4) return launch_pdl(prompt_merge_kernel<8>, mgrid, P_MERGE_THREADS, 0, st, p);
+    return launch_pdl(prompt_merge_kernel<4>, mgrid, P_MERGE_THREADS, 0, st, p);
 }
 
 template <int BITS>

@@ -285,3 +285,22 @@ def test_workspace_reused_across_shapes():
     n = len(probs)
     for a, b in zip(outs[:n], outs[n:]):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [1, 40])
+def test_stacked_with_an_empty_projection(M):
+    """A stack that holds a projection with no rows between two others: the
+    empty one is skipped (nothing to cut, nothing written) and the others
+    give the bits of their separate calls, on both kernels."""
+    bits, group, K = 4, 64, 512
+    (_, c1, s1, b1), w1, xd = packed_problem(bits, group, M, 300, K, seed=61)
+    _, c2, s2, b2 = synth.problem(bits, group, M, 500, K, seed=62)
+    w2 = api.pack(*cuda(c2, s2, b2), bits, group)
+    wn = api.pack(torch.zeros(0, K, dtype=torch.uint8, device="cuda"),
+                  torch.zeros(0, K // group, dtype=torch.bfloat16, device="cuda"),
+                  torch.zeros(0, K // group, dtype=torch.bfloat16, device="cuda"), bits, group)
+    y1, yn, y2 = api.run_stacked([w1, wn, w2], xd)
+    torch.cuda.synchronize()
+    assert yn.shape == (M, 0)
+    assert torch.equal(y1.view(torch.int16), api.run(w1, xd).view(torch.int16))
+    assert torch.equal(y2.view(torch.int16), api.run(w2, xd).view(torch.int16))
