@@ -39,8 +39,10 @@
 // its up block; for a whole tile they meet in shared memory, for a cut tile
 // they count in on one counter; the gate warp, or the last to arrive, stores
 // h = gelu_approx(gate) * up as bf16 operations.
-// Work split ("stream-K"): the projection's blocks, numbered tile-major, are
-// cut into one contiguous run per CTA.  A tile cut by run boundaries gets one
+// Work split: the projection's blocks, numbered tile-major, are cut into one
+// contiguous run per CTA; how many runs (one whole tile each, a whole number
+// per tile, or an even cut of all blocks, "stream-K") is the launch planner's
+// choice (plan.cu).  A tile cut by run boundaries gets one
 // fp32 partial per run; the last warp to arrive (an atomic counter per tile
 // and 16-row group, no waiting) adds them in run order and resets the
 // counter.  The run that holds a tile's first blocks reaches them at its

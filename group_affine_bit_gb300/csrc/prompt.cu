@@ -3,8 +3,9 @@
 //
 // The weights are the A operand and live in tensor memory; the activations
 // are the B operand in shared memory.  One CTA per SM works on a contiguous
-// run of units ("stream-K"); a unit is a 256-row tile pair (two 128-row
-// layout tiles) x one 128-deep block.  Per unit:
+// run of units (an even cut of all units, "stream-K", or a whole number of
+// runs per tile: the launch planner's choice, plan.cu); a unit is a 256-row
+// tile pair (two 128-row layout tiles) x one 128-deep block.  Per unit:
 //   * one producer thread copies the unit's 128 x 128 activation tile (TMA,
 //     two 64-wide panels, 128-byte swizzle, rows past M and depth past K read
 //     as zero) into a ring of activation stages, another the two packed
